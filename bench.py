@@ -1,0 +1,386 @@
+"""Benchmark of the MoE expert block (forward + retention select + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the whole layer (moe_fwd, moe_select_retained when the
+workload has a quota, moe_bwd) on one synthetic batch whose inputs are already
+resident in HBM. Prints ONE JSON line (rank 0). Metric: layer tokens/s
+(fwd+bwd), with the grouped GEMMs' fraction of the measured dense bf16 peak in
+"roofline". Under torchrun (N > 1) every rank runs an independent replica of
+the layer on its own GPU (weak scaling; the layer has no exchange step on one
+GPU's worth of tokens), timing is max over ranks, value = all ranks' tokens / time.
+
+--impl reference times the fp64 oracle (the only other implementation of this
+layer) on the host cores on bounded token samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "qwen3_t4096_full"
+METRIC = "MoE layer fwd+bwd tokens/s (1 GB300); grouped-GEMM % of BF16 tensor peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="oracle time budget for cpu_baseline")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------ work accounting
+def gemm_flops(w, R: int) -> float:
+    """Algorithmic flops of every grouped GEMM of one step (router GEMMs included)."""
+    T, H, F, E, P, Fs = w.T, w.H, w.F, w.E, w.P, w.F_shared
+    f = 2.0 * T * H * E                      # router logits
+    f += 6.0 * P * H * F                     # gate/up (4PHF) + down (2PHF)
+    f += 6.0 * T * H * Fs                    # shared forward
+    f += 6.0 * R * H * F                     # dH (2RHF) + dX_pair (4RHF)
+    f += 6.0 * T * H * Fs                    # shared dH + dX
+    if not w.frozen:
+        f += 6.0 * R * H * F                 # dW gate/up (4RHF) + down (2RHF)
+        f += 2.0 * T * H * E                 # dW router
+        f += 6.0 * T * H * Fs                # shared dW
+    return f
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smmax=float(parts[2]), power=float(parts[3]),
+                                 active=parts[4], hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            if r["hw"].lower() == "active":
+                reasons.add("hw_slowdown")
+            if r["hwt"].lower() == "active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"].lower() == "active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"].lower() == "active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smmax"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows), "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+def oracle_sample_time(w, inp64, n_tokens: int) -> float:
+    """Seconds the fp64 oracle takes for fwd(+select)+bwd on the first n_tokens tokens."""
+    import numpy as np
+
+    from oracle import moe_oracle as O
+
+    sub = dict(inp64)
+    sub["x"] = inp64["x"][:n_tokens]
+    dy = inp64["dy"][:n_tokens]
+    quota = None
+    if w.quota_factor is not None:
+        from expert_grouped_gemm_gb300.inputs import custom
+
+        sub_w = custom(w.name, T=n_tokens, H=w.H, F=w.F, E=w.E, k=w.k, quota_factor=w.quota_factor)
+        quota = np.full(w.E, sub_w.quota_per_expert())
+    t0 = time.perf_counter()
+    f = O.forward(sub, w.k)
+    O.backward(sub, f, dy, quota=quota, frozen=w.frozen)
+    return time.perf_counter() - t0
+
+
+def oracle_inputs64(w, seed):
+    from expert_grouped_gemm_gb300.inputs import bf16_bits_to_f64, make_inputs
+
+    raw = make_inputs(w, seed)
+    return {k: (None if v is None else bf16_bits_to_f64(v)) for k, v in raw.items() if k != "quota"}
+
+
+def cpu_baseline(w, seed, budget_s):
+    """Oracle tokens/s on a bounded token sample sized to roughly budget_s of CPU work."""
+    inp64 = oracle_inputs64(w, seed)
+    n = min(w.T, 64)
+    t = oracle_sample_time(w, inp64, n)
+    if t < budget_s / 4 and n < w.T:
+        n = int(min(w.T, max(n, n * (budget_s / max(t, 1e-3)) * 0.8)))
+        n = max(16, n - n % 16)
+        t = oracle_sample_time(w, inp64, n)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": n / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {w.T} tokens of the same layer (all {w.E} experts, same weights), "
+                      f"fwd+bwd in numpy fp64, {t:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from expert_grouped_gemm_gb300.inputs import WORKLOADS, describe
+
+    w = WORKLOADS[args.workload]
+    inp64 = oracle_inputs64(w, args.seed)
+    steps, warm = args.steps, args.warmup
+    # bounded per-step sample: whole run within ~2 minutes
+    probe = oracle_sample_time(w, inp64, min(w.T, 32))
+    per_step_budget = 120.0 / max(1, steps + warm)
+    n = int(max(8, min(w.T, 32 * per_step_budget / max(probe, 1e-3))))
+    for _ in range(warm):
+        oracle_sample_time(w, inp64, n)
+    tot = 0.0
+    for _ in range(steps):
+        tot += oracle_sample_time(w, inp64, n)
+    value = steps * n / tot
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": steps, "warmup": warm, "ms_per_step": 1000.0 * tot / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, **{k: v for k, v in describe(w).items() if k != "name"}},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n} of {w.T} tokens per step, numpy fp64 oracle fwd+bwd"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from expert_grouped_gemm_gb300 import _lib
+    from expert_grouped_gemm_gb300 import build as b
+    from expert_grouped_gemm_gb300.inputs import WORKLOADS, describe, make_inputs
+    from expert_grouped_gemm_gb300.layer import MoELayer
+
+    if not b.up_to_date():
+        if rank == 0:
+            b.build()
+        if world > 1:
+            torch.distributed.barrier()
+    _lib.load()
+
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, args.seed)
+    layer = MoELayer(w, inp, dev, record_routing=True)
+    x = inp["x"].to(dev)
+    dy = inp["dy"].to(dev)
+    quota = inp["quota"].to(dev) if inp["quota"] is not None else None
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        layer.step(x, dy, quota)
+    torch.cuda.synchronize()
+    if _lib.moe_read_status(layer.ws) != 0:
+        raise RuntimeError("device status not OK after warm-up")
+    R = int(layer.ret_offsets[-1].item()) if quota is not None else w.P
+    counts = torch.diff(layer.offsets).cpu()
+
+    # ---- timed region: K steps, inputs resident in HBM
+    clocks = ClockSampler(torch.cuda.current_device())
+    _lib.moe_timing_read()
+    _lib.moe_timing_enable(True)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    n0 = _lib.moe_kernel_launches()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        layer.step(x, dy, quota)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    n1 = _lib.moe_kernel_launches()
+    barrier()
+    clk = clocks.stop()
+    _lib.moe_timing_enable(False)
+    fam_ms, fam_n = _lib.moe_timing_read()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * w.T * args.steps / (ms / 1e3)
+
+    # ---- end to end through the public API: pinned host inputs in, results out
+    hx = torch.empty_like(inp["x"]).pin_memory()
+    hx.copy_(inp["x"])
+    hdy = torch.empty_like(inp["dy"]).pin_memory()
+    hdy.copy_(inp["dy"])
+    hq = inp["quota"].pin_memory() if quota is not None else None
+    hy = torch.empty_like(hx).pin_memory()
+    hdx = torch.empty_like(hx).pin_memory()
+    dx_dev = torch.empty_like(x)
+    dy_dev = torch.empty_like(dy)
+    q_dev = torch.empty_like(quota) if quota is not None else None
+    e2e_steps = max(1, min(args.steps, 100))
+
+    def e2e_step():
+        dx_dev.copy_(hx, non_blocking=True)
+        dy_dev.copy_(hdy, non_blocking=True)
+        if q_dev is not None:
+            q_dev.copy_(hq, non_blocking=True)
+        layer.step(dx_dev, dy_dev, q_dev)
+        hy.copy_(layer.y, non_blocking=True)
+        hdx.copy_(layer.dx, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ems = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ems], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ems = float(t.item())
+    e2e_value = world * w.T * e2e_steps / (ems / 1e3)
+    h2d = hx.numel() * hx.element_size() + hdy.numel() * hdy.element_size() + (
+        hq.numel() * hq.element_size() if hq is not None else 0)
+    d2h = hy.numel() * hy.element_size() + hdx.numel() * hdx.element_size()
+
+    if world > 1:
+        torch.distributed.barrier()
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return 0
+
+    peaks, src = load_peaks()
+    gemm_ms_step = fam_ms[0] / args.steps
+    flops = gemm_flops(w, R)
+    achieved = flops / (gemm_ms_step / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": None, "kernel": "tc_grouped_gemm (all grouped-GEMM launches of one step)",
+            "peak_source": f"{src} bf16_tflops (burst)", "gemm_ms_per_step": gemm_ms_step,
+            "bw_kernels_ms_per_step": fam_ms[1] / args.steps, "gemm_flops_per_step": flops}
+    traffic_file = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(traffic_file):
+        tr = json.load(open(traffic_file)).get(w.name)
+        if tr and tr.get("kernel_hash") == kernel_hash():
+            roof["traffic"] = tr["bytes_per_step"]
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded N(0,1) tokens/grads, N(0,0.02) weights, Zipf router bias)",
+            "config": {"workload": w.name, **{k: v for k, v in describe(w).items() if k != "name"},
+                       "R_retained_rows": R, "expert_load_max": int(counts.max()),
+                       "expert_load_min": int(counts.min()), "zero_load_experts": int((counts == 0).sum()),
+                       "l2": "no flush: per-step working set > L2 (expert weights alone are "
+                             f"{3 * w.E * w.H * w.F * 2 / 1e9:.2f} GB, read twice per step)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "gpu_launches": int(n1 - n0), "clocks": clk,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "roofline": roof}
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, args.seed, args.cpu_budget_s)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def kernel_hash() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in ("gemm_tc.cu", "epilogue.cuh", "common.cuh", "gemm.h"):
+        h.update(open(os.path.join(ROOT, "expert_grouped_gemm_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

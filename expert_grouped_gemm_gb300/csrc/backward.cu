@@ -1,0 +1,440 @@
+// backward.cu -- backward bandwidth kernels of the MoE block.
+//
+// Pair scores, quota selection and compaction follow "LRMoE: Demand-Side Load
+// Re-Calibration for Efficient MoE Training on Memory-Constrained Nodes"
+// (arXiv 2610.37720), Abstract: every token-expert pair gets a score that
+// estimates its contribution to the expert update, each expert keeps the
+// pairs within its quota, and the kept pairs are physically compacted so the
+// backward grouped GEMMs run on smaller, variable-size groups. The metric
+// itself is not given there; the score used is w * ||dY_t||_2 * ||x_t||_2.
+// Ranking inside an expert is (score descending, token ascending); kept rows
+// stay in row (= token) order.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ pair scores
+// Warp per padded row r: g[r] = <dY_t, y_r>, score[r] = w ||dY_t|| ||x_t||, and
+// (full mode) dy_perm[r] = w dY_t; pad rows of dy_perm are zeroed.
+template <typename TIO>
+__global__ void __launch_bounds__(256) k_pair_score(const TIO* dy, const TIO* y_pair, const int* pair_of_row,
+                                                    const int* pad_total, const float* topk_w, const float* xnorm,
+                                                    int H, int k, float* g, float* score, TIO* dy_perm,
+                                                    float* user_scores) {
+  const int nrows = *pad_total;
+  const int lane = threadIdx.x & 31;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < nrows; r += (gridDim.x * blockDim.x) >> 5) {
+    const int p = pair_of_row[r];
+    if (p < 0) {
+      if (dy_perm) {
+        TIO* dst = dy_perm + (int64_t)r * H;
+        for (int i = lane; i < H; i += 32) dst[i] = TIO(0);
+      }
+      continue;
+    }
+    const int t = p / k;
+    const float w = topk_w[p];
+    const TIO* dyr = dy + (int64_t)t * H;
+    const TIO* yr = y_pair + (int64_t)r * H;
+    TIO* dst = dy_perm ? dy_perm + (int64_t)r * H : nullptr;
+    float ss = 0.0f, dot = 0.0f;
+    if constexpr (sizeof(TIO) == 2) {
+      for (int i = lane; i < H / 8; i += 32) {
+        float a[8], b[8];
+        bf16x8_to_f(reinterpret_cast<const uint4*>(dyr)[i], a);
+        bf16x8_to_f(reinterpret_cast<const uint4*>(yr)[i], b);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          ss = fmaf(a[q], a[q], ss);
+          dot = fmaf(a[q], b[q], dot);
+          a[q] *= w;
+        }
+        if (dst) reinterpret_cast<uint4*>(dst)[i] = f_to_bf16x8(a);
+      }
+    } else {
+      for (int i = lane; i < H; i += 32) {
+        const float a = io<TIO>::to_f(dyr[i]);
+        ss = fmaf(a, a, ss);
+        dot = fmaf(a, io<TIO>::to_f(yr[i]), dot);
+        if (dst) dst[i] = io<TIO>::cvt(w * a);
+      }
+    }
+    ss = warp_sum(ss);
+    dot = warp_sum(dot);
+    if (lane == 0) {
+      const float s = w * sqrtf(ss) * xnorm[t];
+      g[r] = dot;
+      score[r] = s;
+      if (user_scores) user_scores[p] = s;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ quota select
+__device__ __forceinline__ uint64_t sel_key(float s, int local) {
+  uint32_t u = __float_as_uint(s);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // order-preserving
+  return ((uint64_t)u << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)local);
+}
+
+// Block per expert (256 threads). Finds the q-th largest (score, -token) key by
+// an 8-pass MSB-first radix select over 8-bit digits, keeps keys >= it, and
+// numbers the kept rows in row order.
+__global__ void __launch_bounds__(256) k_select(const float* score, const int* count, const int* pad_off,
+                                                const int* quota, int* ret_cidx, int* ret_count, int* status) {
+  __shared__ int hist[256];
+  __shared__ uint64_t s_prefix, s_mask;
+  __shared__ int s_need;
+  __shared__ int s_carry;
+  const int e = blockIdx.x;
+  const int cnt = count[e];
+  const int base = pad_off[e];
+  int q = cnt;
+  if (quota) {
+    const int qq = quota[e];
+    if (qq < 0 && threadIdx.x == 0) set_status(status, MOE_ERR_DEVICE_ARG);
+    q = min(max(qq, 0), cnt);
+  }
+  uint64_t thr = 0;  // keep keys >= thr
+  bool keep_all = (q == cnt), keep_none = (q == 0);
+  if (!keep_all && !keep_none) {
+    if (threadIdx.x == 0) {
+      s_prefix = 0;
+      s_mask = 0;
+      s_need = q;
+    }
+    __syncthreads();
+    for (int d = 56; d >= 0; d -= 8) {
+      hist[threadIdx.x] = 0;
+      __syncthreads();
+      const uint64_t pre = s_prefix, msk = s_mask;
+      for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+        const uint64_t key = sel_key(score[base + i], i);
+        if ((key & msk) == pre) atomicAdd(&hist[(key >> d) & 0xFF], 1);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int need = s_need, acc = 0, b = 255;
+        for (; b > 0; --b) {
+          if (acc + hist[b] >= need) break;
+          acc += hist[b];
+        }
+        s_need = need - acc;
+        s_prefix = pre | ((uint64_t)b << d);
+        s_mask = msk | (0xFFull << d);
+      }
+      __syncthreads();
+    }
+    thr = s_prefix;
+  }
+  // number kept rows in row order
+  if (threadIdx.x == 0) s_carry = 0;
+  __syncthreads();
+  for (int i0 = 0; i0 < cnt; i0 += blockDim.x) {
+    const int i = i0 + threadIdx.x;
+    bool kept = false;
+    if (i < cnt) kept = keep_all || (!keep_none && sel_key(score[base + i], i) >= thr);
+    int tot;
+    const int pos = block_excl_scan(kept ? 1 : 0, &tot);
+    if (i < cnt) ret_cidx[base + i] = kept ? s_carry + pos : -1;
+    __syncthreads();
+    if (threadIdx.x == 0) s_carry += tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) ret_count[e] = q;
+}
+
+// One block of 1024 threads: offsets of the kept rows, exact and padded.
+__global__ void __launch_bounds__(1024) k_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off,
+                                                   int* ret_tile_off, int* ret_src, int* user_offsets) {
+  const int e = threadIdx.x;
+  const int cnt = e < E ? ret_count[e] : 0;
+  const int pad = (cnt + 15) / 16 * 16;
+  const int tiles = (cnt + 127) / 128;
+  int tc, tp, tt;
+  const int oc = block_excl_scan(cnt, &tc);
+  const int op = block_excl_scan(pad, &tp);
+  const int ot = block_excl_scan(tiles, &tt);
+  if (e < E) {
+    ret_offset[e] = oc;
+    ret_pad_off[e] = op;
+    ret_tile_off[e] = ot;
+    if (user_offsets) user_offsets[e] = oc;
+    for (int r = op + cnt; r < op + pad; ++r) ret_src[r] = -1;
+  }
+  if (e == 0) {
+    ret_offset[E] = tc;
+    ret_pad_off[E] = tp;
+    ret_tile_off[E] = tt;
+    if (user_offsets) user_offsets[E] = tc;
+  }
+}
+
+// Thread per pair: compact row of each kept pair and the exposed kept-row list.
+__global__ void k_ret_index(const int* topk_idx, const int* rowp_of_pair, const int* row_of_pair,
+                            const int* ret_cidx, const int* ret_offset, const int* ret_pad_off, int64_t P,
+                            int* ret_src, int* crow_of_pair, int* ret_rows, int* user_rows) {
+  for (int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; p < P; p += (int64_t)gridDim.x * blockDim.x) {
+    const int r = rowp_of_pair[p];
+    const int c = ret_cidx[r];
+    if (c >= 0) {
+      const int e = topk_idx[p];
+      const int crow = ret_pad_off[e] + c;
+      ret_src[crow] = r;
+      crow_of_pair[p] = crow;
+      ret_rows[ret_offset[e] + c] = row_of_pair[p];
+      if (user_rows) user_rows[ret_offset[e] + c] = row_of_pair[p];
+    } else {
+      crow_of_pair[p] = -1;
+    }
+  }
+}
+
+// Warp per compact row: copy x_t, a|b, h of the kept pair and write w dY_t.
+template <typename TIO>
+__device__ __forceinline__ void copy_row(TIO* dst, const TIO* src, int n, int lane) {
+  if constexpr (sizeof(TIO) == 2) {
+    for (int i = lane; i < n / 8; i += 32) reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+  } else {
+    for (int i = lane; i < n; i += 32) dst[i] = src[i];
+  }
+}
+template <typename TIO>
+__device__ __forceinline__ void zero_row(TIO* dst, int n, int lane) {
+  if constexpr (sizeof(TIO) == 2) {
+    for (int i = lane; i < n / 8; i += 32) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
+  } else {
+    for (int i = lane; i < n; i += 32) dst[i] = TIO(0);
+  }
+}
+
+template <typename TIO>
+__global__ void __launch_bounds__(256) k_compact_rows(const int* ret_src, const int* ret_pad_total,
+                                                      const int* pair_of_row, const float* topk_w, const TIO* x,
+                                                      const TIO* ab, const TIO* h, const TIO* dy, int H, int F, int k,
+                                                      TIO* x_c, TIO* ab_c, TIO* h_c, TIO* dy_c) {
+  const int nrows = *ret_pad_total;
+  const int lane = threadIdx.x & 31;
+  for (int c = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; c < nrows; c += (gridDim.x * blockDim.x) >> 5) {
+    const int src = ret_src[c];
+    TIO* xd = x_c + (int64_t)c * H;
+    TIO* abd = ab_c + (int64_t)c * 2 * F;
+    TIO* hd = h_c + (int64_t)c * F;
+    TIO* dyd = dy_c + (int64_t)c * H;
+    if (src < 0) {
+      zero_row(xd, H, lane);
+      zero_row(abd, 2 * F, lane);
+      zero_row(hd, F, lane);
+      zero_row(dyd, H, lane);
+      continue;
+    }
+    const int p = pair_of_row[src];
+    const int t = p / k;
+    const float w = topk_w[p];
+    copy_row(xd, x + (int64_t)t * H, H, lane);
+    copy_row(abd, ab + (int64_t)src * 2 * F, 2 * F, lane);
+    copy_row(hd, h + (int64_t)src * F, F, lane);
+    const TIO* dyr = dy + (int64_t)t * H;
+    if constexpr (sizeof(TIO) == 2) {
+      for (int i = lane; i < H / 8; i += 32) {
+        float a[8];
+        bf16x8_to_f(reinterpret_cast<const uint4*>(dyr)[i], a);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) a[q] *= w;
+        reinterpret_cast<uint4*>(dyd)[i] = f_to_bf16x8(a);
+      }
+    } else {
+      for (int i = lane; i < H; i += 32) dyd[i] = io<TIO>::cvt(w * io<TIO>::to_f(dyr[i]));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ router backward
+// Warp per token: dl_j = w_j (g_j - sum_i w_i g_i); dense row of dl (zeros off the
+// selection) for the dW_router GEMM; rows in [T, Tpad) are zeroed.
+template <typename TIO>
+__global__ void __launch_bounds__(256) k_router_bwd(const float* g, const int* rowp_of_pair, const int* topk_idx,
+                                                    const float* topk_w, int T, int Tpad, int E, int k,
+                                                    float* dl_sel, TIO* dl_dense) {
+  const int lane = threadIdx.x & 31;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tpad; t += (gridDim.x * blockDim.x) >> 5) {
+    if (t >= T) {
+      if (dl_dense)
+        for (int e = lane; e < E; e += 32) dl_dense[(int64_t)t * E + e] = TIO(0);
+      continue;
+    }
+    const int64_t p0 = (int64_t)t * k;
+    float mean = 0.0f;
+    for (int j = 0; j < k; ++j) mean = fmaf(topk_w[p0 + j], g[rowp_of_pair[p0 + j]], mean);
+    if (lane == 0)
+      for (int j = 0; j < k; ++j) dl_sel[p0 + j] = topk_w[p0 + j] * (g[rowp_of_pair[p0 + j]] - mean);
+    if (dl_dense) {
+      for (int e = lane; e < E; e += 32) {
+        float v = 0.0f;
+        for (int j = 0; j < k; ++j)
+          if (topk_idx[p0 + j] == e) v = topk_w[p0 + j] * (g[rowp_of_pair[p0 + j]] - mean);
+        dl_dense[(int64_t)t * E + e] = io<TIO>::cvt(v);
+      }
+    }
+  }
+}
+
+// 32x32 tiled transpose: out[c][r] = in[r][c], in is [R, Cc].
+template <typename TIO>
+__global__ void k_transpose(const TIO* in, int R, int Cc, TIO* out) {
+  __shared__ TIO tile[32][33];
+  const int bx = blockIdx.x * 32, by = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int r = by + i, c = bx + threadIdx.x;
+    if (r < R && c < Cc) tile[i][threadIdx.x] = in[(int64_t)r * Cc + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int c = bx + i, r = by + threadIdx.x;
+    if (r < R && c < Cc) out[(int64_t)c * R + r] = tile[threadIdx.x][i];
+  }
+}
+
+// ------------------------------------------------------------------ dX reduce
+// Warp per token: dX_t = sum_j [kept] dx_pair[crow(t,j)] + sum_j dl_j W_r[:,e_j] (+ shared dX_t).
+template <typename TIO>
+__global__ void __launch_bounds__(256) k_dx_reduce(const TIO* dx_pair, const int* crow_of_pair, const int* topk_idx,
+                                                   const float* dl_sel, const TIO* wrT, const TIO* sh_dx, int T, int H,
+                                                   int k, TIO* dx) {
+  const int lane = threadIdx.x & 31;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
+    const int64_t p0 = (int64_t)t * k;
+    TIO* dst = dx + (int64_t)t * H;
+    if constexpr (sizeof(TIO) == 2) {
+      for (int i = lane; i < H / 8; i += 32) {
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, f[8];
+        for (int j = 0; j < k; ++j) {
+          const int cr = crow_of_pair[p0 + j];
+          if (cr < 0) continue;
+          bf16x8_to_f(reinterpret_cast<const uint4*>(dx_pair + (int64_t)cr * H)[i], f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] += f[q];
+        }
+        for (int j = 0; j < k; ++j) {
+          const float d = dl_sel[p0 + j];
+          bf16x8_to_f(reinterpret_cast<const uint4*>(wrT + (int64_t)topk_idx[p0 + j] * H)[i], f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = fmaf(d, f[q], acc[q]);
+        }
+        if (sh_dx) {
+          bf16x8_to_f(reinterpret_cast<const uint4*>(sh_dx + (int64_t)t * H)[i], f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] += f[q];
+        }
+        reinterpret_cast<uint4*>(dst)[i] = f_to_bf16x8(acc);
+      }
+    } else {
+      for (int i = lane; i < H; i += 32) {
+        float acc = 0.0f;
+        for (int j = 0; j < k; ++j) {
+          const int cr = crow_of_pair[p0 + j];
+          if (cr >= 0) acc += io<TIO>::to_f(dx_pair[(int64_t)cr * H + i]);
+        }
+        for (int j = 0; j < k; ++j)
+          acc = fmaf(dl_sel[p0 + j], io<TIO>::to_f(wrT[(int64_t)topk_idx[p0 + j] * H + i]), acc);
+        if (sh_dx) acc += io<TIO>::to_f(sh_dx[(int64_t)t * H + i]);
+        dst[i] = io<TIO>::cvt(acc);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+static int grid_for(int64_t warps, int num_sms) {
+  const int64_t want = (warps + 7) / 8;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 16));
+}
+
+template <typename TIO>
+cudaError_t launch_pair_score(const void* dy, const void* y_pair, const int* pair_of_row, const int* pad_total,
+                              int64_t Rmax, const float* topk_w, const float* xnorm, int H, int k, float* g,
+                              float* score, void* dy_perm, float* user_scores, int num_sms, cudaStream_t st) {
+  k_pair_score<TIO><<<grid_for(Rmax, num_sms), 256, 0, st>>>(
+      reinterpret_cast<const TIO*>(dy), reinterpret_cast<const TIO*>(y_pair), pair_of_row, pad_total, topk_w, xnorm,
+      H, k, g, score, reinterpret_cast<TIO*>(dy_perm), user_scores);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select(const float* score, const int* count, const int* pad_off, const int* quota, int E,
+                          int* ret_cidx, int* ret_count, int* status, cudaStream_t st) {
+  k_select<<<E, 256, 0, st>>>(score, count, pad_off, quota, ret_cidx, ret_count, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off, int* ret_tile_off,
+                            int* ret_src, int* user_offsets, cudaStream_t st) {
+  k_ret_scan<<<1, 1024, 0, st>>>(ret_count, E, ret_offset, ret_pad_off, ret_tile_off, ret_src, user_offsets);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ret_index(const int* topk_idx, const int* rowp_of_pair, const int* row_of_pair,
+                             const int* ret_cidx, const int* ret_offset, const int* ret_pad_off, int64_t P,
+                             int* ret_src, int* crow_of_pair, int* ret_rows, int* user_rows, int num_sms,
+                             cudaStream_t st) {
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((P + 255) / 256, (int64_t)num_sms * 8));
+  k_ret_index<<<grid, 256, 0, st>>>(topk_idx, rowp_of_pair, row_of_pair, ret_cidx, ret_offset, ret_pad_off, P,
+                                    ret_src, crow_of_pair, ret_rows, user_rows);
+  return cudaGetLastError();
+}
+
+template <typename TIO>
+cudaError_t launch_compact_rows(const int* ret_src, const int* ret_pad_total, int64_t Rmax, const int* pair_of_row,
+                                const float* topk_w, const void* x, const void* ab, const void* h, const void* dy,
+                                int H, int F, int k, void* x_c, void* ab_c, void* h_c, void* dy_c, int num_sms,
+                                cudaStream_t st) {
+  k_compact_rows<TIO><<<grid_for(Rmax, num_sms), 256, 0, st>>>(
+      ret_src, ret_pad_total, pair_of_row, topk_w, reinterpret_cast<const TIO*>(x), reinterpret_cast<const TIO*>(ab),
+      reinterpret_cast<const TIO*>(h), reinterpret_cast<const TIO*>(dy), H, F, k, reinterpret_cast<TIO*>(x_c),
+      reinterpret_cast<TIO*>(ab_c), reinterpret_cast<TIO*>(h_c), reinterpret_cast<TIO*>(dy_c));
+  return cudaGetLastError();
+}
+
+template <typename TIO>
+cudaError_t launch_router_bwd(const float* g, const int* rowp_of_pair, const int* topk_idx, const float* topk_w,
+                              int T, int Tpad, int E, int k, float* dl_sel, void* dl_dense, int num_sms,
+                              cudaStream_t st) {
+  k_router_bwd<TIO><<<grid_for(Tpad, num_sms), 256, 0, st>>>(g, rowp_of_pair, topk_idx, topk_w, T, Tpad, E, k,
+                                                             dl_sel, reinterpret_cast<TIO*>(dl_dense));
+  return cudaGetLastError();
+}
+
+template <typename TIO>
+cudaError_t launch_transpose(const void* in, int R, int Cc, void* out, cudaStream_t st) {
+  dim3 grid((Cc + 31) / 32, (R + 31) / 32), block(32, 8);
+  k_transpose<TIO><<<grid, block, 0, st>>>(reinterpret_cast<const TIO*>(in), R, Cc, reinterpret_cast<TIO*>(out));
+  return cudaGetLastError();
+}
+
+template <typename TIO>
+cudaError_t launch_dx_reduce(const void* dx_pair, const int* crow_of_pair, const int* topk_idx, const float* dl_sel,
+                             const void* wrT, const void* sh_dx, int T, int H, int k, void* dx, int num_sms,
+                             cudaStream_t st) {
+  k_dx_reduce<TIO><<<grid_for(T, num_sms), 256, 0, st>>>(
+      reinterpret_cast<const TIO*>(dx_pair), crow_of_pair, topk_idx, dl_sel, reinterpret_cast<const TIO*>(wrT),
+      reinterpret_cast<const TIO*>(sh_dx), T, H, k, reinterpret_cast<TIO*>(dx));
+  return cudaGetLastError();
+}
+
+#define MOE_INST(TIO)                                                                                               \
+  template cudaError_t launch_pair_score<TIO>(const void*, const void*, const int*, const int*, int64_t,           \
+                                              const float*, const float*, int, int, float*, float*, void*, float*, \
+                                              int, cudaStream_t);                                                  \
+  template cudaError_t launch_compact_rows<TIO>(const int*, const int*, int64_t, const int*, const float*,         \
+                                                const void*, const void*, const void*, const void*, int, int, int, \
+                                                void*, void*, void*, void*, int, cudaStream_t);                    \
+  template cudaError_t launch_router_bwd<TIO>(const float*, const int*, const int*, const float*, int, int, int,   \
+                                              int, float*, void*, int, cudaStream_t);                              \
+  template cudaError_t launch_transpose<TIO>(const void*, int, int, void*, cudaStream_t);                          \
+  template cudaError_t launch_dx_reduce<TIO>(const void*, const int*, const int*, const float*, const void*,       \
+                                             const void*, int, int, int, void*, int, cudaStream_t);
+MOE_INST(float)
+MOE_INST(__nv_bfloat16)
+#undef MOE_INST
+
+}  // namespace moe

@@ -1,0 +1,284 @@
+// route.cu -- forward bandwidth kernels: top-k routing, deterministic
+// histogram + scan, stable permutation, row gather and weighted combine.
+//
+// Routing follows issue "[MoE] Hot experts on RNGD during training (host
+// dispatch, device expert graphs) #14", Proposal (routing and dispatch of
+// token rows to experts, results scattered back), done here on the device:
+//   * selection: per token the k largest biased fp32 logits, ties to the lower
+//     expert index, slots in that order; weights = softmax renormalised over
+//     the k selected logits, i.e. exp(l_j - l_max) / sum_j' exp(l_j' - l_max);
+//   * placement: expert-contiguous rows, token order inside an expert, each
+//     expert padded to 16 rows. Per 64-token chunk, a 64-bit mask per expert
+//     records which tokens chose it, so a pair's rank inside its expert is a
+//     popcount: no atomics on rows, identical result on every run.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kChunk = 64;  // tokens per routing chunk (one bit each in a uint64 mask)
+
+// ------------------------------------------------------------------ top-k
+// grid = C chunks, block = 256 (8 warps); warp per token.
+__global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* bias, int T, int E, int k,
+                                                    int* topk_idx, float* topk_w, uint64_t* masks) {
+  extern __shared__ uint64_t smask[];  // [E]
+  const int c = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) smask[e] = 0ull;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int tl = warp; tl < kChunk; tl += 8) {
+    const int t = c * kChunk + tl;
+    if (t >= T) break;
+    float* lrow = logits + (int64_t)t * E;
+    for (int e = lane; e < E; e += 32) lrow[e] = lrow[e] + (bias ? bias[e] : 0.0f);
+    __syncwarp();
+    uint32_t taken = 0;  // bit i: expert lane + 32 i already selected
+    float lmax = 0.0f, sum = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+      for (int i = 0, e = lane; e < E; ++i, e += 32) {
+        if ((taken >> i) & 1u) continue;
+        float v = lrow[e];
+        if (v != v) v = -INFINITY;  // NaN ranks last
+        if (be == 0x7fffffff || v > bv || (v == bv && e < be)) {
+          bv = v;
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (lane == 0) {
+        if (j == 0) lmax = bv;
+        const float ex = expf(bv - lmax);
+        sum += ex;
+        topk_idx[(int64_t)t * k + j] = be;
+        topk_w[(int64_t)t * k + j] = ex;
+        atomicOr(reinterpret_cast<unsigned long long*>(&smask[be]), 1ull << tl);
+      }
+    }
+    if (lane == 0) {
+      const float inv = 1.0f / sum;
+      for (int j = 0; j < k; ++j) topk_w[(int64_t)t * k + j] *= inv;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) masks[(int64_t)c * E + e] = smask[e];
+}
+
+// ------------------------------------------------------------------ scan
+// One block of 1024 threads, thread e = expert e.
+__global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset,
+                                                     int* pad_off, int* tile_off, int* chunk_base, int* pair_of_row,
+                                                     int* user_offsets) {
+  const int e = threadIdx.x;
+  int cnt = 0;
+  if (e < E)
+    for (int c = 0; c < C; ++c) cnt += __popcll(masks[(int64_t)c * E + e]);
+  const int pad = (cnt + 15) / 16 * 16;
+  const int tiles = (cnt + 127) / 128;
+  int tot_c, tot_p, tot_t;
+  const int oc = block_excl_scan(e < E ? cnt : 0, &tot_c);
+  const int op = block_excl_scan(e < E ? pad : 0, &tot_p);
+  const int ot = block_excl_scan(e < E ? tiles : 0, &tot_t);
+  if (e < E) {
+    count[e] = cnt;
+    offset[e] = oc;
+    pad_off[e] = op;
+    tile_off[e] = ot;
+    if (user_offsets) user_offsets[e] = oc;
+    int run = op;
+    for (int c = 0; c < C; ++c) {
+      chunk_base[(int64_t)c * E + e] = run;
+      run += __popcll(masks[(int64_t)c * E + e]);
+    }
+    for (int r = op + cnt; r < op + pad; ++r) pair_of_row[r] = -1;
+  }
+  if (e == 0) {
+    offset[E] = tot_c;
+    pad_off[E] = tot_p;
+    tile_off[E] = tot_t;
+    if (user_offsets) user_offsets[E] = tot_c;
+  }
+}
+
+// ------------------------------------------------------------------ pair -> row
+// grid = C chunks, block = 256.
+__global__ void __launch_bounds__(256) k_route_index(const uint64_t* masks, const int* chunk_base, const int* topk_idx,
+                                                     const int* offset, const int* pad_off, int T, int E, int k,
+                                                     int* rowp_of_pair, int* row_of_pair, int* pair_of_row) {
+  extern __shared__ uint64_t sm[];  // masks[E] then bases[E]
+  int* sbase = reinterpret_cast<int*>(sm + E);
+  const int c = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    sm[e] = masks[(int64_t)c * E + e];
+    sbase[e] = chunk_base[(int64_t)c * E + e];
+  }
+  __syncthreads();
+  const int t0 = c * kChunk;
+  const int ntok = min(kChunk, T - t0);
+  for (int i = threadIdx.x; i < ntok * k; i += blockDim.x) {
+    const int tl = i / k;
+    const int64_t p = (int64_t)t0 * k + i;
+    const int e = topk_idx[p];
+    const int rank = __popcll(sm[e] & ((1ull << tl) - 1ull));
+    const int prow = sbase[e] + rank;
+    rowp_of_pair[p] = prow;
+    row_of_pair[p] = offset[e] + (prow - pad_off[e]);
+    pair_of_row[prow] = (int)p;
+  }
+}
+
+// ------------------------------------------------------------------ gather
+// Warp per padded row: x_perm[r] = x[token(r)] (zeros for pad rows); the warp
+// that copies slot 0 of a token also writes ||x_t||_2.
+template <typename TIO>
+__global__ void __launch_bounds__(256) k_gather_rows(const TIO* x, const int* pair_of_row, const int* pad_total,
+                                                     int H, int k, TIO* x_perm, float* xnorm) {
+  const int nrows = *pad_total;
+  const int lane = threadIdx.x & 31;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < nrows; r += (gridDim.x * blockDim.x) >> 5) {
+    const int p = pair_of_row[r];
+    TIO* dst = x_perm + (int64_t)r * H;
+    float ss = 0.0f;
+    if constexpr (sizeof(TIO) == 2) {
+      const int nv = H / 8;
+      if (p < 0) {
+        for (int i = lane; i < nv; i += 32) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)(p / k) * H);
+        for (int i = lane; i < nv; i += 32) {
+          const uint4 u = src[i];
+          reinterpret_cast<uint4*>(dst)[i] = u;
+          float f[8];
+          bf16x8_to_f(u, f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
+        }
+      }
+    } else {
+      if (p < 0) {
+        for (int i = lane; i < H; i += 32) dst[i] = TIO(0);
+      } else {
+        const TIO* src = x + (int64_t)(p / k) * H;
+        for (int i = lane; i < H; i += 32) {
+          const float v = io<TIO>::to_f(src[i]);
+          dst[i] = src[i];
+          ss = fmaf(v, v, ss);
+        }
+      }
+    }
+    if (p >= 0 && (p % k) == 0) {
+      ss = warp_sum(ss);
+      if (lane == 0) xnorm[p / k] = sqrtf(ss);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ combine
+// Warp per token: y[t] = sum_j w[t,j] y_pair[row(t,j)] (+ shared y[t]), slots ascending.
+template <typename TIO>
+__global__ void __launch_bounds__(256) k_combine(const TIO* y_pair, const int* rowp_of_pair, const float* topk_w,
+                                                 const TIO* sh_y, int T, int H, int k, TIO* y) {
+  const int lane = threadIdx.x & 31;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
+    TIO* dst = y + (int64_t)t * H;
+    if constexpr (sizeof(TIO) == 2) {
+      const int nv = H / 8;
+      for (int i = lane; i < nv; i += 32) {
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int j = 0; j < k; ++j) {
+          const float w = topk_w[(int64_t)t * k + j];
+          const int r = rowp_of_pair[(int64_t)t * k + j];
+          float f[8];
+          bf16x8_to_f(reinterpret_cast<const uint4*>(y_pair + (int64_t)r * H)[i], f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = fmaf(w, f[q], acc[q]);
+        }
+        if (sh_y) {
+          float f[8];
+          bf16x8_to_f(reinterpret_cast<const uint4*>(sh_y + (int64_t)t * H)[i], f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] += f[q];
+        }
+        reinterpret_cast<uint4*>(dst)[i] = f_to_bf16x8(acc);
+      }
+    } else {
+      for (int i = lane; i < H; i += 32) {
+        float acc = 0.0f;
+        for (int j = 0; j < k; ++j) {
+          const float w = topk_w[(int64_t)t * k + j];
+          const int r = rowp_of_pair[(int64_t)t * k + j];
+          acc = fmaf(w, io<TIO>::to_f(y_pair[(int64_t)r * H + i]), acc);
+        }
+        if (sh_y) acc += io<TIO>::to_f(sh_y[(int64_t)t * H + i]);
+        dst[i] = io<TIO>::cvt(acc);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, int k, int* topk_idx, float* topk_w,
+                              uint64_t* masks, cudaStream_t st) {
+  const int C = (T + kChunk - 1) / kChunk;
+  k_route_topk<<<C, 256, E * sizeof(uint64_t), st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset, int* pad_off,
+                              int* tile_off, int* chunk_base, int* pair_of_row, int* user_offsets, cudaStream_t st) {
+  k_route_scan<<<1, 1024, 0, st>>>(masks, C, E, count, offset, pad_off, tile_off, chunk_base, pair_of_row,
+                                   user_offsets);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_index(const uint64_t* masks, const int* chunk_base, const int* topk_idx, const int* offset,
+                               const int* pad_off, int T, int E, int k, int* rowp_of_pair, int* row_of_pair,
+                               int* pair_of_row, cudaStream_t st) {
+  const int C = (T + kChunk - 1) / kChunk;
+  const size_t sm = E * (sizeof(uint64_t) + sizeof(int));
+  k_route_index<<<C, 256, sm, st>>>(masks, chunk_base, topk_idx, offset, pad_off, T, E, k, rowp_of_pair, row_of_pair,
+                                    pair_of_row);
+  return cudaGetLastError();
+}
+
+template <typename TIO>
+cudaError_t launch_gather_rows(const void* x, const int* pair_of_row, const int* pad_total, int64_t Rmax, int H, int k,
+                               void* x_perm, float* xnorm, int num_sms, cudaStream_t st) {
+  const int64_t want = (Rmax + 7) / 8;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 16));
+  k_gather_rows<TIO><<<grid, 256, 0, st>>>(reinterpret_cast<const TIO*>(x), pair_of_row, pad_total, H, k,
+                                           reinterpret_cast<TIO*>(x_perm), xnorm);
+  return cudaGetLastError();
+}
+
+template <typename TIO>
+cudaError_t launch_combine(const void* y_pair, const int* rowp_of_pair, const float* topk_w, const void* sh_y, int T,
+                           int H, int k, void* y, int num_sms, cudaStream_t st) {
+  const int64_t want = ((int64_t)T + 7) / 8;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 16));
+  k_combine<TIO><<<grid, 256, 0, st>>>(reinterpret_cast<const TIO*>(y_pair), rowp_of_pair, topk_w,
+                                       reinterpret_cast<const TIO*>(sh_y), T, H, k, reinterpret_cast<TIO*>(y));
+  return cudaGetLastError();
+}
+
+template cudaError_t launch_gather_rows<float>(const void*, const int*, const int*, int64_t, int, int, void*, float*,
+                                               int, cudaStream_t);
+template cudaError_t launch_gather_rows<__nv_bfloat16>(const void*, const int*, const int*, int64_t, int, int, void*,
+                                                       float*, int, cudaStream_t);
+template cudaError_t launch_combine<float>(const void*, const int*, const float*, const void*, int, int, int, void*,
+                                           int, cudaStream_t);
+template cudaError_t launch_combine<__nv_bfloat16>(const void*, const int*, const float*, const void*, int, int, int,
+                                                   void*, int, cudaStream_t);
+
+}  // namespace moe

@@ -1,0 +1,136 @@
+"""GPU parity of the whole MoE block (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from expert_grouped_gemm_gb300 import _lib
+from expert_grouped_gemm_gb300.inputs import WORKLOADS, custom, make_inputs
+from tests.parity import parity_case, run_gpu, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib_loaded():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    _lib.load()
+
+
+# --------------------------------------------------------------- small and ragged shapes
+MEDIUM = dict(T=300, H=256, F=192, E=16, k=4, zipf_s=1.0)
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("tiny_f32", None),
+    ("medium_bf16_full", dict(MEDIUM, F_shared=128)),
+    ("medium_bf16_frozen", dict(MEDIUM, frozen=True)),
+    ("medium_bf16_retained", dict(MEDIUM, F_shared=128, quota_factor=0.5)),
+    ("medium_bf16_quota_small", dict(MEDIUM, quota_factor=0.1)),
+    ("ragged_tail", dict(T=77, H=192, F=320, E=32, k=3, zipf_s=1.5, zero_experts=3, quota_factor=0.5)),
+    ("k1", dict(T=129, H=128, F=128, E=16, k=1, zipf_s=0.5)),
+    ("k_equals_E", dict(T=40, H=128, F=64, E=16, k=16)),
+    ("single_token", dict(T=1, H=128, F=128, E=16, k=2, F_shared=64)),
+    ("f32_ragged", dict(T=45, H=40, F=24, E=5, k=2, dtype="f32", zipf_s=1.0, quota_factor=0.5, F_shared=8)),
+])
+def test_parity_small(name, kw):
+    w = WORKLOADS[name] if kw is None else custom(name, **kw)
+    rep, *_ = parity_case(w, seed=1)
+    print(name, rep)
+
+
+def test_all_tokens_to_one_expert():
+    w = custom("one_expert", T=200, H=128, F=128, E=16, k=1)
+    inp = make_inputs(w, seed=2)
+    bias = torch.full((16,), -50.0)
+    bias[5] = 50.0
+    inp["router_bias"] = bias
+    rep, g, *_ = parity_case(w, inp=inp)
+    assert g["offsets"][6] - g["offsets"][5] == 200
+
+
+def test_quota_zero_everywhere():
+    w = custom("q0", T=100, H=128, F=128, E=16, k=2, zipf_s=1.0)
+    inp = make_inputs(w, seed=3)
+    inp["quota"] = torch.zeros(16, dtype=torch.int32)
+    rep, g, *_ = parity_case(w, inp=inp)
+    assert g["ret_offsets"][-1] == 0
+    for n in ("dw_gate", "dw_up", "dw_down"):
+        assert np.all(g[n] == 0.0)
+
+
+# --------------------------------------------------------------- determinism and keep-all
+def test_bitwise_determinism_and_keep_all_equals_full():
+    w = custom("det", T=512, H=256, F=256, E=32, k=4, zipf_s=1.2, F_shared=128)
+    inp = make_inputs(w, seed=4)
+    g1, layer = run_gpu(w, inp, use_quota=False)
+    g2, _ = run_gpu(w, inp, use_quota=False, layer=layer)
+    for n in ("Y", "dX", "dw_gate", "dw_up", "dw_down", "dw_router", "dws_gate"):
+        assert np.array_equal(g1[n], g2[n]), n
+    # quota >= every count keeps every pair: compacted backward must equal the full one bitwise
+    inp_all = dict(inp)
+    inp_all["quota"] = torch.full((w.E,), w.T, dtype=torch.int32)
+    g3, _ = run_gpu(w, inp_all, use_quota=True, layer=layer)
+    assert g3["ret_offsets"][-1] == w.P
+    for n in ("dX", "dw_gate", "dw_up", "dw_down", "dw_router", "dws_gate", "dws_up", "dws_down"):
+        assert np.array_equal(g1[n], g3[n]), n
+
+
+# --------------------------------------------------------------- device-side argument errors
+def test_negative_quota_sets_device_status():
+    w = custom("negq", T=64, H=128, F=128, E=16, k=2)
+    inp = make_inputs(w, seed=5)
+    layer_inp = dict(inp)
+    from expert_grouped_gemm_gb300.layer import MoELayer
+    layer = MoELayer(w, layer_inp, record_routing=True)
+    x, dy = inp["x"].cuda(), inp["dy"].cuda()
+    layer.forward(x)
+    q = torch.full((16,), 3, dtype=torch.int32, device="cuda")
+    q[7] = -1
+    layer.select(dy, q)
+    assert _lib.moe_read_status(layer.ws) == _lib.MOE_ERR_DEVICE_ARG
+    assert _lib.moe_read_status(layer.ws) == _lib.MOE_OK  # cleared by the read
+    layer.backward(dy, x, True)
+    assert _lib.moe_read_status(layer.ws) == _lib.MOE_OK
+
+
+def test_call_order_errors_on_device():
+    w = custom("order", T=64, H=128, F=128, E=16, k=2)
+    inp = make_inputs(w, seed=6)
+    from expert_grouped_gemm_gb300.layer import MoELayer
+    layer = MoELayer(w, inp)
+    x, dy = inp["x"].cuda(), inp["dy"].cuda()
+    with pytest.raises(_lib.MoeError) as ei:
+        layer.backward(dy, x, False)
+    assert ei.value.code == _lib.MOE_ERR_STATE
+    layer.forward(x)
+    x2 = x.clone()
+    with pytest.raises(_lib.MoeError) as ei:
+        layer.backward(dy, x2, False)
+    assert ei.value.code == _lib.MOE_ERR_STATE
+    with pytest.raises(_lib.MoeError) as ei:
+        layer.backward(dy, x, True)  # no selection yet
+    assert ei.value.code == _lib.MOE_ERR_STATE
+    layer.backward(dy, x, False)
+    assert _lib.moe_read_status(layer.ws) == _lib.MOE_OK
+
+
+# --------------------------------------------------------------- full-size workloads
+@pytest.mark.parametrize("name", [
+    "qwen3_t128_frozen",
+    "qwen3_t4096_full",
+    "qwen3_t4096_retained_s0.5",
+    "qwen3_t4096_retained_s1.0",
+    "qwen3_t4096_retained_s1.5",
+])
+def test_parity_full_size_qwen(name):
+    rep, *_ = parity_case(WORKLOADS[name], seed=0)
+    print(name, rep)
+
+
+@pytest.mark.parametrize("name", ["glm45_t8192_full", "glm45_t8192_retained"])
+def test_parity_full_size_glm(name):
+    rep, g, *_ = parity_case(WORKLOADS[name], seed=0)
+    cnt = np.diff(g["offsets"])
+    assert np.sum(cnt == 0) >= 1, "expected some zero-token experts"
+    print(name, rep)
