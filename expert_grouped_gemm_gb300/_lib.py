@@ -30,7 +30,7 @@ MOE_FROZEN = 1
 
 EXPORTED = ["moe_workspace_size", "moe_fwd", "moe_select_retained", "moe_bwd", "moe_read_status",
             "moe_last_error", "moe_workspace_entry", "moe_kernel_launches", "moe_timing_enable",
-            "moe_timing_read"]
+            "moe_timing_read", "moe_route_noalloc"]
 
 
 class MoeError(RuntimeError):
@@ -67,6 +67,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.moe_last_error.restype = ctypes.c_char_p
     lib.moe_workspace_entry.argtypes = [D, ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
                                         ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_route_noalloc.argtypes = [D, vp, vp, vp, vp, i32p, f32p, i32p, i32p, i32p]
+    lib.moe_route_noalloc.restype = ctypes.c_int
     lib.moe_kernel_launches.argtypes = []
     lib.moe_kernel_launches.restype = ctypes.c_int64
     lib.moe_timing_enable.argtypes = [ctypes.c_int]
@@ -159,6 +161,18 @@ def moe_bwd(dims: Dims, ws: torch.Tensor, dy, x, use_retained, dx, dw_router=Non
         _ptr(dw_router, "dw_router", io, False), _ptr(dw_gate, "dw_gate", io, False), _ptr(dw_up, "dw_up", io, False),
         _ptr(dw_down, "dw_down", io, False), _ptr(dws_gate, "dws_gate", io, False),
         _ptr(dws_up, "dws_up", io, False), _ptr(dws_down, "dws_down", io, False))
+    _check(rc)
+
+
+def moe_route_noalloc(dims: Dims, x, w_router, router_bias, topk_idx, topk_w, expert_offsets, row_of_pair,
+                      device_status=None, stream=None):
+    """Routing stage of moe_fwd with no allocation and no workspace (fixed device scratch inside the library)."""
+    io = _io_dtype(dims)
+    rc = load().moe_route_noalloc(
+        ctypes.byref(dims), _stream(stream), _ptr(x, "x", io), _ptr(w_router, "w_router", io),
+        _ptr(router_bias, "router_bias", torch.float32, False), _ptr(topk_idx, "topk_idx", torch.int32),
+        _ptr(topk_w, "topk_w", torch.float32), _ptr(expert_offsets, "expert_offsets", torch.int32),
+        _ptr(row_of_pair, "row_of_pair", torch.int32), _ptr(device_status, "device_status", torch.int32, False))
     _check(rc)
 
 

@@ -281,6 +281,13 @@ GemmArgs base_args(int* status) {
 
 }  // namespace
 
+// Hooks for the other translation units of the library (not part of the C ABI).
+namespace moe {
+int internal_check_dims(const moe_dims* d) { return check_dims(d); }
+int internal_fail(int code, const char* msg) { return fail(code, "%s", msg); }
+void internal_count_launches(int n) { g_launches += n; }
+}  // namespace moe
+
 // ====================================================================== C ABI
 extern "C" {
 

@@ -167,6 +167,37 @@ MOE_API int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* strea
             void* dws_gate, void* dws_up, void* dws_down);
 
 /*
+ * moe_route_noalloc -- the routing stage of moe_fwd without any device
+ * allocation and without a workspace. It is for callers that cannot call
+ * cudaMalloc or lend the library memory: a runtime whose device memory pool
+ * is fixed up front, a plugin that must not touch its host's allocator, a
+ * process held to a pre-sized memory budget. The pages this library follows
+ * have no counterpart to it; it exists only for those callers.
+ *   Computes the same values moe_fwd reports through its optional outputs:
+ *   router logits x w_router + router_bias (fp32), top-k experts per token
+ *   (ties to the lower index), softmax-renormalised weights, per-expert
+ *   exclusive offsets and the expert-contiguous row of every pair.
+ * Inputs:  x[T,H], w_router[H,E] (dims.dtype), router_bias[E] float (nullable).
+ * Outputs (all required, device): topk_idx[T,k] int32, topk_w[T,k] float,
+ *          expert_offsets[E+1] int32, row_of_pair[T*k] int32;
+ *          device_status (nullable, one int32 on the device): set to MOE_OK,
+ *          or to MOE_ERR_TIMEOUT if a bounded wait inside a kernel ran out.
+ * Scratch: one fixed array of 8 MiB in the library's device memory (every
+ *          GPU that loads the library holds it until the process exits).
+ *          Dims whose scratch would not fit (roughly T*E > 1,048,576 at
+ *          k <= 8) are rejected with MOE_ERR_UNSUPPORTED before any work.
+ *          Every call on a device uses the same array and leaves its
+ *          contents behind: calls that overlap on the GPU (two streams, or
+ *          two threads without ordering) race on it and must be serialised.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Calls no cudaMalloc/cudaFree or allocating library routine.
+ */
+MOE_API int moe_route_noalloc(const moe_dims* dims, void* stream, const void* x, const void* w_router,
+                              const float* router_bias, int32_t* topk_idx, float* topk_w,
+                              int32_t* expert_offsets, int32_t* row_of_pair, int32_t* device_status);
+
+/*
  * moe_read_status -- synchronises `stream` and returns the device status word
  * of the workspace (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_ARG), then
  * clears it. Returns MOE_ERR_CUDA if the synchronisation itself failed.
