@@ -147,9 +147,10 @@ __global__ void __launch_bounds__(256) k_select(const float* score, const int* c
 
 // One block of 1024 threads: offsets of the kept rows, exact and padded.
 __global__ void __launch_bounds__(1024) k_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off,
-                                                   int* ret_tile_off, int* ret_src, int* user_offsets) {
+                                                   int* ret_tile_off, int* ret_src, int* user_offsets, int* order) {
   const int e = threadIdx.x;
   const int cnt = e < E ? ret_count[e] : 0;
+  if (order) block_order_desc(cnt, E, order);
   const int pad = (cnt + 15) / 16 * 16;
   const int tiles = (cnt + 127) / 128;
   int tc, tp, tt;
@@ -368,8 +369,8 @@ cudaError_t launch_select(const float* score, const int* count, const int* pad_o
 }
 
 cudaError_t launch_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off, int* ret_tile_off,
-                            int* ret_src, int* user_offsets, cudaStream_t st) {
-  k_ret_scan<<<1, 1024, 0, st>>>(ret_count, E, ret_offset, ret_pad_off, ret_tile_off, ret_src, user_offsets);
+                            int* ret_src, int* user_offsets, cudaStream_t st, int* order) {
+  k_ret_scan<<<1, 1024, 0, st>>>(ret_count, E, ret_offset, ret_pad_off, ret_tile_off, ret_src, user_offsets, order);
   return cudaGetLastError();
 }
 

@@ -57,6 +57,8 @@ struct GemmArgs {
   const void* aux;
   int64_t ld_aux;
   int zero_pad;         // var-M: write zeros in rows [rows_g, round16(rows_g))
+  int64_t out_rows;     // rows of the out0 / out1 2-D views (tensor-core stores are clipped there)
+  const int* g_order;   // var-K: order in which groups are scheduled (heaviest first), or null
   int* status;
 };
 

@@ -2,15 +2,23 @@
 //
 // Per CTA (192 threads, one CTA per SM):
 //   warp 0      TMA producer: loads A/B k-blocks of 64 into a STAGES-deep
-//               ring of 128-byte-swizzled shared-memory tiles.
+//               ring of 128-byte-swizzled shared-memory tiles. An MN-major
+//               operand (row-major [K, MN]) is read through a 3-D view
+//               (64 columns, K rows, column chunk) so one bulk-tensor copy
+//               fills all of its 64-column chunks.
 //   warp 1      MMA issuer: tcgen05.mma (M=128, N=BN, K=16) into one of two
 //               tensor-memory accumulators, commits free smem slots back.
 //   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (one row per
-//               thread), fused epilogue (SwiGLU fwd/bwd, store, dW), global stores.
-// Tiles (group, m-block, n-block) are read from device-side group offsets, so
-// the host never learns the per-expert row counts. Every barrier wait is
-// bounded; a wait that runs out sets MOE_ERR_TIMEOUT in the status word, the
-// CTA drains its own copies and MMAs, frees its tensor memory and returns.
+//               thread), fused epilogue (SwiGLU fwd/bwd, store, dW), then the
+//               results go through a 128-byte-swizzled staging tile in shared
+//               memory and out with TMA bulk tensor stores of 32 rows x 64
+//               columns (16 rows at a group's padded end, which is a multiple
+//               of 16, so a store never reaches into another group's rows).
+// Tiles (group, m-block, n-block) come from device-side group offsets, so the
+// host never learns the per-group row counts. Variable-K groups are visited
+// heaviest first. Every barrier wait is bounded; a wait that runs out sets
+// MOE_ERR_TIMEOUT in the status word, the CTA drains its own copies and MMAs,
+// frees its tensor memory and returns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -21,16 +29,19 @@
 namespace moe {
 
 constexpr int kThreads = 192;
+constexpr int kStageRowBytes = 128;                   // 64 bf16 per staged row
+constexpr int kStageTileBytes = 32 * kStageRowBytes;  // one warp's 32 rows x 64 columns (4 KB)
 
-template <int BN>
+template <int BN, int STAGES, int EPI_WARP_BYTES>
 struct TcCfg {
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr int A_BYTES = kTileM * kTileK * 2;  // 16 KB
   static constexpr int B_BYTES = BN * kTileK * 2;      // 32 KB (BN=256) / 16 KB
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = EPI_OFF + 4 * EPI_WARP_BYTES;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;  // barriers + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 2 * BN;      // two accumulators
+  static constexpr bool MN3D = (BN == 256);           // MN-major operands through 3-D views
 };
 
 struct TileInfo {
@@ -48,8 +59,9 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int NT
   TileInfo ti;
   if (a.var_k) {
     const int MT = (a.M + kTileM - 1) / kTileM;
-    ti.g = t / (MT * NT);
-    const int rem = t - ti.g * MT * NT;
+    const int gi = t / (MT * NT);
+    const int rem = t - gi * MT * NT;
+    ti.g = a.g_order ? a.g_order[gi] : gi;
     ti.m0 = (rem / NT) * kTileM;
     ti.nt = rem % NT;
     ti.rows = grp_rows(a, ti.g);
@@ -86,16 +98,42 @@ __device__ __forceinline__ int total_tiles(const GemmArgs& a) {
   return mt * NT;
 }
 
-template <int BN>
+// ---------------------------------------------------------------- epilogue pieces
+// Byte offset of 16-byte chunk j (0..7) of row r in a 128-byte-swizzled staging
+// tile: the layout a TMA store with 128-byte swizzle reads.
+__device__ __forceinline__ uint32_t stage_off(int r, int j) { return r * kStageRowBytes + ((j ^ (r & 7)) << 4); }
+
+// SwiGLU backward: coalesced asynchronous copy of the a|b values of one
+// 64-column chunk for one warp's 32 rows (eight threads per row, 16 bytes each)
+// into the (a tile, b tile) pair at `buf`; rows at or past `rows_left` are skipped.
+__device__ __forceinline__ void aux_prefetch(uint32_t buf, const __nv_bfloat16* ab, int64_t row0, int64_t ld, int N,
+                                             int n0, int rows_left, int lane) {
+  if (n0 < N) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = (lane >> 3) + 4 * i, j = lane & 7;
+      if (r < rows_left) {
+        const __nv_bfloat16* src = ab + (row0 + r) * ld + n0 + 8 * j;
+        cp_async16(buf + stage_off(r, j), src);
+        cp_async16(buf + kStageTileBytes + stage_off(r, j), src + N);
+      }
+    }
+  }
+  cp_async_commit();
+}
+
+template <int BN, int STAGES, int EPI_WARP_BYTES>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                    const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
-  using C = TcCfg<BN>;
+                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
+                    const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO0h,
+                    const __grid_constant__ CUtensorMap tmO1h, const GemmArgs args) {
+  using C = TcCfg<BN, STAGES, EPI_WARP_BYTES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint64_t* empty = full + C::STAGES;
-  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -105,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -133,9 +171,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB1);
     int stage = 0;
     uint32_t phase = 0;
-    int issued_parity[C::STAGES];
+    int issued_parity[STAGES];
 #pragma unroll
-    for (int s = 0; s < C::STAGES; ++s) issued_parity[s] = -1;
+    for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const TileInfo ti = decode_tile<BN>(args, t, NT);
@@ -149,43 +187,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t fb = smem_u32(&full[stage]);
         mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
         issued_parity[stage] = (int)phase;
+        // A
         if (!args.var_k) {
           tma_load_2d(smem_u32(sa), &tmA, fb, kb * kTileK, ti.off + ti.m0);
+        } else if (C::MN3D) {
+          tma_load_3d(smem_u32(sa), &tmA, fb, 0, ti.off + kb * kTileK, ti.m0 / 64);
         } else {
           tma_load_2d(smem_u32(sa), &tmA, fb, ti.m0, ti.off + kb * kTileK);
           tma_load_2d(smem_u32(sa + 8192), &tmA, fb, ti.m0 + 64, ti.off + kb * kTileK);
         }
+        // B
         if (args.b_kmajor) {
           const bool second = args.k_split > 0 && kb * kTileK >= args.k_split;
           const int kk = second ? kb - args.k_split / kTileK : kb;
           tma_load_2d(smem_u32(sb), second ? &tmB1 : &tmB0, fb, kk * kTileK, ti.g * args.N + ti.nt * BN);
         } else {
           const int brow = args.var_k ? ti.off + kb * kTileK : ti.g * args.K + kb * kTileK;
-#pragma unroll
-          for (int c = 0; c < BN / 64; ++c) {
-            int col;
-            const CUtensorMap* map = &tmB0;
-            if (args.paired) {
-              const int half = c / (BN / 128);
-              col = ti.nt * (BN / 2) + (c % (BN / 128)) * 64;
-              if (half) {
-                map = &tmB1;
-                col += args.b1_col;
-              }
+          if (C::MN3D) {
+            if (args.paired) {  // two halves of BN/2 columns: B0 then B1 (at column offset b1_col)
+              tma_load_3d(smem_u32(sb), &tmB0, fb, 0, brow, ti.nt * (BN / 128));
+              tma_load_3d(smem_u32(sb + BN / 2 * 128), &tmB1, fb, 0, brow, args.b1_col / 64 + ti.nt * (BN / 128));
             } else {
-              col = ti.nt * BN + c * 64;
+              tma_load_3d(smem_u32(sb), &tmB0, fb, 0, brow, ti.nt * (BN / 64));
             }
-            tma_load_2d(smem_u32(sb + c * 8192), map, fb, col, brow);
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c) {
+              int col;
+              const CUtensorMap* map = &tmB0;
+              if (args.paired) {
+                const int half = c / (BN / 128);
+                col = ti.nt * (BN / 2) + (c % (BN / 128)) * 64;
+                if (half) {
+                  map = &tmB1;
+                  col += args.b1_col;
+                }
+              } else {
+                col = ti.nt * BN + c * 64;
+              }
+              tma_load_2d(smem_u32(sb + c * 8192), map, fb, col, brow);
+            }
           }
         }
-        if (++stage == C::STAGES) {
+        if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
     // make sure no copy of ours is still landing in shared memory
-    for (int s = 0; s < C::STAGES; ++s)
+    for (int s = 0; s < STAGES; ++s)
       if (issued_parity[s] >= 0) mbar_wait_timed(&full[s], (uint32_t)issued_parity[s], 200000000ull);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -219,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
         }
         tc_commit(&empty[stage]);
-        if (++stage == C::STAGES) {
+        if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
@@ -233,46 +284,163 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_timed(drain, 0, 200000000ull);
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
     const int row = q * 32 + lane;
+    const uint32_t wstage = smem_u32(smem + C::EPI_OFF + (warp - 2) * EPI_WARP_BYTES);
+    const bool tma_out = args.epi != EPI_F32;
+    const bool bwd = args.epi == EPI_SWIGLU_BWD;
+    const bool fwd = args.epi == EPI_SWIGLU_FWD;
+    const int nout = fwd ? 3 : ((bwd || (args.epi == EPI_DW && args.paired)) ? 2 : 1);
+    // one output alternates two staging sets when room allows; otherwise one set
+    const int nbuf = (nout == 1 && EPI_WARP_BYTES >= 2 * kStageTileBytes) ? 2 : 1;
+    const uint32_t aux_buf = wstage + 2 * kStageTileBytes;  // SwiGLU bwd: a and b tiles of one chunk
+    const int W = args.paired ? BN / 2 : BN;                // output columns per tile
+    const int CW = W / 64;                                  // 64-column chunks per tile
+    const __nv_bfloat16* ab_aux = reinterpret_cast<const __nv_bfloat16*>(args.aux);
     int acc_i = 0;
-    float v0[32], v1[32];
+    int sc = 0;  // staging sets used so far by this warp
+    uint32_t ra[32], rb[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) rb[i] = 0u;  // only paired modes load it
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const TileInfo ti = decode_tile<BN>(args, t, NT);
       const int m = ti.m0 + row;
-      if (ti.kblocks == 0) {  // variable-K group with no rows: its output is zero
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v0[i] = v1[i] = 0.0f;
-        if (args.paired) {
-          for (int c = 0; c < BN / 64; ++c)
-            epilogue_apply<__nv_bfloat16, 32>(args, ti.g, ti.rows, m, ti.nt * (BN / 2) + c * 32, v0, v1);
-        } else {
-          for (int c = 0; c < BN / 32; ++c)
-            epilogue_apply<__nv_bfloat16, 32>(args, ti.g, ti.rows, m, ti.nt * BN + c * 32, v0, nullptr);
-        }
-        continue;
-      }
-      const int acc = acc_i & 1;
-      const uint32_t acc_par = (uint32_t)((acc_i >> 1) & 1);
-      if (!mbar_wait_bounded(&tfull[acc], acc_par, abort_flag)) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      if (args.paired) {
-        for (int c = 0; c < BN / 64; ++c) {
-          tmem_ld32(taddr + c * 32, v0);
-          tmem_ld32(taddr + BN / 2 + c * 32, v1);
-          epilogue_apply<__nv_bfloat16, 32>(args, ti.g, ti.rows, m, ti.nt * (BN / 2) + c * 32, v0, v1);
-        }
+      const int ncol0 = ti.nt * W;
+      // rows of this tile that may be written, and the output row of this warp's box
+      int lim;
+      int64_t out_row0;
+      if (args.var_k) {
+        lim = args.M - ti.m0;
+        out_row0 = (int64_t)ti.g * args.M + ti.m0 + q * 32;
       } else {
-        for (int c = 0; c < BN / 32; ++c) {
-          tmem_ld32(taddr + c * 32, v0);
-          epilogue_apply<__nv_bfloat16, 32>(args, ti.g, ti.rows, m, ti.nt * BN + c * 32, v0, nullptr);
+        lim = round_pad(ti.rows) - ti.m0;
+        out_row0 = (int64_t)ti.off + ti.m0 + q * 32;
+      }
+      const int rows_left = lim - q * 32;                    // rows of this warp's 32 that are written
+      const bool real = args.var_k || m < ti.rows;           // var-M rows past the group end are zero padding
+      const int64_t aux_row0 = (int64_t)ti.off + ti.m0 + q * 32;
+      if (bwd) aux_prefetch(aux_buf, ab_aux, aux_row0, args.ld_aux, args.N, ncol0, rows_left, lane);
+      const bool empty_tile = ti.kblocks == 0;  // variable-K group with no rows: output is zero
+      const int acc = acc_i & 1;
+      if (!empty_tile) {
+        const uint32_t acc_par = (uint32_t)((acc_i >> 1) & 1);
+        if (!mbar_wait_bounded(&tfull[acc], acc_par, abort_flag)) break;
+        tc_fence_after();
+      }
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      const bool live = !empty_tile && real;
+      for (int c = 0; c < CW; ++c) {
+        const int n0 = ncol0 + c * 64;
+        const bool store = rows_left > 0 && n0 < args.N;
+        uint32_t set = wstage;
+        if (tma_out && store) {
+          set = wstage + (nbuf == 2 ? (uint32_t)((sc & 1) * kStageTileBytes) : 0u);
+          // the set must be free: the bulk stores that last used it have read it
+          if (lane == 0) {
+            if (nbuf == 2) bulk_wait_read_but1(); else bulk_wait_read_all();
+          }
+          __syncwarp();
+        }
+        if (bwd) {  // a|b of this chunk has landed
+          cp_async_wait<0>();
+          __syncwarp();
+        }
+        for (int hh = 0; hh < 2; ++hh) {  // two 32-column halves of the chunk
+          if (!empty_tile) {
+            tmem_ld32_async(taddr + c * 64 + hh * 32, ra);
+            if (args.paired) {  // gate and up columns of this half under one wait
+              tmem_ld32_async(taddr + BN / 2 + c * 64 + hh * 32, rb);
+              tmem_ld_wait(ra);
+              tmem_ld_order(rb);
+            } else {
+              tmem_ld_wait(ra);
+            }
+          }
+          if (!tma_out) {  // fp32 logits (single group): direct 16-byte stores, one row per thread
+            const int nh = n0 + hh * 32;
+            if (!empty_tile && m < ti.rows && nh < args.N) {
+              float* o = reinterpret_cast<float*>(args.out0) + ((int64_t)ti.off + m) * args.ldo + nh;
+              const int nv = min(32, args.N - nh);
+              if (nv == 32 && (reinterpret_cast<uintptr_t>(o) & 15) == 0) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                  *reinterpret_cast<uint4*>(o + i) = make_uint4(ra[i], ra[i + 1], ra[i + 2], ra[i + 3]);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (i < nv) o[i] = __uint_as_float(ra[i]);
+              }
+            }
+            continue;
+          }
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8) {
+            const int j = hh * 4 + g8;  // 16-byte chunk of the staged 128-byte row
+            float x0[8], x1[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              x0[i] = live ? __uint_as_float(ra[8 * g8 + i]) : 0.0f;
+              x1[i] = live ? __uint_as_float(rb[8 * g8 + i]) : 0.0f;
+            }
+            if (fwd) {
+              float h[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) h[i] = x0[i] * sigmoidf_(x0[i]) * x1[i];
+              if (store) {
+                st_shared_v4(set + stage_off(lane, j), f_to_bf16x8(x0));
+                st_shared_v4(set + kStageTileBytes + stage_off(lane, j), f_to_bf16x8(x1));
+                st_shared_v4(set + 2 * kStageTileBytes + stage_off(lane, j), f_to_bf16x8(h));
+              }
+            } else if (bwd) {
+              float av[8], bv[8], da[8], db[8];
+              bf16x8_to_f(ld_shared_v4(aux_buf + stage_off(lane, j)), av);
+              bf16x8_to_f(ld_shared_v4(aux_buf + kStageTileBytes + stage_off(lane, j)), bv);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float s = sigmoidf_(av[i]);
+                da[i] = x0[i] * bv[i] * s * (1.0f + av[i] * (1.0f - s));
+                db[i] = x0[i] * av[i] * s;
+              }
+              if (store) {
+                st_shared_v4(set + stage_off(lane, j), f_to_bf16x8(da));
+                st_shared_v4(set + kStageTileBytes + stage_off(lane, j), f_to_bf16x8(db));
+              }
+            } else if (store) {  // EPI_DW / EPI_STORE
+              st_shared_v4(set + stage_off(lane, j), f_to_bf16x8(x0));
+              if (nout > 1) st_shared_v4(set + kStageTileBytes + stage_off(lane, j), f_to_bf16x8(x1));
+            }
+          }
+        }
+        if (!tma_out) continue;
+        if (bwd) {  // a|b of the next chunk lands while this one is stored
+          __syncwarp();
+          if (c + 1 < CW) aux_prefetch(aux_buf, ab_aux, aux_row0, args.ld_aux, args.N, n0 + 64, rows_left, lane);
+        }
+        if (!store) continue;
+        ++sc;
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          // a | b (or da | db) go to the two halves of one a|b row; dW_up next to dW_gate
+          const bool ab_row = fwd || bwd;
+          const int c1 = ab_row ? args.N + n0 : n0;
+          const bool full_box = rows_left >= 32;  // else a 16-row box ends at the group's padded end
+          const CUtensorMap* o0 = full_box ? &tmO0 : &tmO0h;
+          const CUtensorMap* o1 = ab_row ? o0 : (full_box ? &tmO1 : &tmO1h);
+          tma_store_2d(o0, set, n0, (int)out_row0);
+          if (nout > 1) tma_store_2d(o1, set + kStageTileBytes, c1, (int)out_row0);
+          if (nout > 2) tma_store_2d(full_box ? &tmO1 : &tmO1h, set + 2 * kStageTileBytes, n0, (int)out_row0);
+          bulk_commit();
         }
       }
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
-      ++acc_i;
+      if (!empty_tile) {
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        ++acc_i;
+      }
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   __syncthreads();
@@ -298,50 +466,102 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 view [rows, cols] (cols contiguous), box [box_rows, box_cols], 128-byte swizzle,
-// out-of-bounds elements read as zero.
-static bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows) {
+// 2-D bf16 view [rows, cols] (cols contiguous) with box [box_rows, box_cols], 128-byte
+// swizzle; out-of-bounds elements read as zero and are dropped on store.
+static bool make_map_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
   cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
-static cudaError_t launch_bn(const GemmArgs& a, cudaStream_t st, int num_sms, int max_tiles_hint) {
-  using C = TcCfg<BN>;
-  cudaError_t e = cudaFuncSetAttribute(tc_grouped_gemm<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+// 3-D view of a row-major [rows, cols] bf16 matrix (cols a multiple of 64):
+// (64 columns, row, 64-column chunk) with strides (2 B, cols*2 B, 128 B).
+// A box (64, box_rows, box_chunks) lands in shared memory as box_chunks
+// consecutive [box_rows][64] tiles: the MN-major operand layout.
+static bool make_map_mn3d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows, int box_chunks) {
+  auto fn = encode_fn();
+  if (!fn || cols % 64) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_chunks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, int EPI_WARP_BYTES>
+static cudaError_t launch_cfg(const GemmArgs& a, cudaStream_t st, int num_sms) {
+  using C = TcCfg<BN, STAGES, EPI_WARP_BYTES>;
+  static_assert(C::SMEM <= 232448, "shared memory budget");
+  auto kern = tc_grouped_gemm<BN, STAGES, EPI_WARP_BYTES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  CUtensorMap mA, mB0, mB1;
+  CUtensorMap mA, mB0, mB1, mO0, mO1, mO0h, mO1h;
   bool ok;
   if (!a.var_k)
-    ok = make_map(&mA, a.A, a.a_rows, a.lda, 64, kTileM);
+    ok = make_map_2d(&mA, a.A, a.a_rows, a.lda, 64, kTileM);
+  else if (C::MN3D)
+    ok = make_map_mn3d(&mA, a.A, a.a_rows, a.lda, kTileK, kTileM / 64);
   else
-    ok = make_map(&mA, a.A, a.a_rows, a.lda, 64, kTileK);
+    ok = make_map_2d(&mA, a.A, a.a_rows, a.lda, 64, kTileK);
+  const void* b1 = a.B1 ? a.B1 : a.B0;
   if (a.b_kmajor) {
-    ok = ok && make_map(&mB0, a.B0, a.b_rows, a.ldb, 64, BN);
-    ok = ok && make_map(&mB1, a.B1 ? a.B1 : a.B0, a.b_rows, a.ldb, 64, BN);
+    ok = ok && make_map_2d(&mB0, a.B0, a.b_rows, a.ldb, 64, BN);
+    ok = ok && make_map_2d(&mB1, b1, a.b_rows, a.ldb, 64, BN);
+  } else if (C::MN3D) {
+    const int chunks = a.paired ? BN / 128 : BN / 64;
+    ok = ok && make_map_mn3d(&mB0, a.B0, a.b_rows, a.ldb, kTileK, chunks);
+    ok = ok && make_map_mn3d(&mB1, b1, a.b_rows, a.ldb, kTileK, chunks);
   } else {
-    ok = ok && make_map(&mB0, a.B0, a.b_rows, a.ldb, 64, kTileK);
-    ok = ok && make_map(&mB1, a.B1 ? a.B1 : a.B0, a.b_rows, a.ldb, 64, kTileK);
+    ok = ok && make_map_2d(&mB0, a.B0, a.b_rows, a.ldb, 64, kTileK);
+    ok = ok && make_map_2d(&mB1, b1, a.b_rows, a.ldb, 64, kTileK);
+  }
+  if (a.epi == EPI_F32) {
+    mO0 = mO1 = mO0h = mO1h = mA;  // unused: fp32 outputs are stored directly
+  } else {
+    // output views: [out_rows, ld] for permuted / single-group outputs, [G*M, ld] for dW
+    const int64_t orows = a.var_k ? (int64_t)a.G * a.M : a.out_rows;
+    const void* o1 = a.out1 ? a.out1 : a.out0;
+    const int64_t ld1 = (a.epi == EPI_SWIGLU_FWD) ? a.ldo1 : a.ldo;
+    ok = ok && make_map_2d(&mO0, a.out0, orows, a.ldo, 64, 32) && make_map_2d(&mO0h, a.out0, orows, a.ldo, 64, 16);
+    ok = ok && make_map_2d(&mO1, o1, orows, ld1, 64, 32) && make_map_2d(&mO1h, o1, orows, ld1, 64, 16);
   }
   if (!ok) return cudaErrorInvalidValue;
-  int grid = num_sms;
-  if (max_tiles_hint > 0 && max_tiles_hint < grid) grid = max_tiles_hint;
-  if (grid < 1) grid = 1;
-  tc_grouped_gemm<BN><<<grid, kThreads, C::SMEM, st>>>(mA, mB0, mB1, a);
+  kern<<<num_sms, kThreads, C::SMEM, st>>>(mA, mB0, mB1, mO0, mO1, mO0h, mO1h, a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_sms, int max_tiles_hint) {
-  if (bn == 256) return launch_bn<256>(a, st, num_sms, max_tiles_hint);
-  return launch_bn<128>(a, st, num_sms, max_tiles_hint);
+// Staging bytes one epilogue warp needs: nout 4 KB tiles (one output with room
+// for two alternates two sets), plus an a|b tile pair for the SwiGLU backward.
+static int staging_bytes(const GemmArgs& a) {
+  if (a.epi == EPI_F32) return 0;
+  if (a.epi == EPI_SWIGLU_FWD) return 3 * kStageTileBytes;
+  if (a.epi == EPI_SWIGLU_BWD) return 2 * kStageTileBytes + 2 * kStageTileBytes;
+  return ((a.epi == EPI_DW && a.paired) ? 2 : 1) * kStageTileBytes;
+}
+
+cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_sms, int /*max_tiles_hint*/) {
+  const int need = staging_bytes(a);
+  if (bn == 128) {
+    constexpr int kEpi = kStageTileBytes;
+    if (a.epi == EPI_SWIGLU_BWD || a.epi == EPI_SWIGLU_FWD || need > kEpi) return cudaErrorInvalidValue;
+    return launch_cfg<128, 6, kEpi>(a, st, num_sms);
+  }
+  if (a.epi == EPI_SWIGLU_BWD || a.epi == EPI_SWIGLU_FWD) {
+    constexpr int kEpi = 4 * kStageTileBytes;
+    if (need > kEpi) return cudaErrorInvalidValue;
+    return launch_cfg<256, 3, kEpi>(a, st, num_sms);
+  }
+  constexpr int kEpi = 2 * kStageTileBytes;
+  if (need > kEpi) return cudaErrorInvalidValue;
+  return launch_cfg<256, 4, kEpi>(a, st, num_sms);
 }
 
 }  // namespace moe

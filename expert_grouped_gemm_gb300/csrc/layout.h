@@ -55,6 +55,8 @@ struct WsPtrs {
   void* wrT;            // [E,H] router weight transposed
   void* sh_dab;         // [Tpad,2Fs]
   void* sh_dx;          // [Tpad,H]
+  int* order;           // [E] experts by count, descending (dW scheduling order)
+  int* ret_order;       // [E] experts by kept count, descending
 };
 
 struct WsLayout {

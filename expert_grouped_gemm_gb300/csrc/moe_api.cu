@@ -103,6 +103,7 @@ WsLayout make_layout(const moe_dims* d) {
       R * 2 * F * es, R * H * es,  // dab dx_pair
       Tp * E * es, T * k * 4, E * H * es,  // dl dl_sel wrT
       Tp * 2 * Fs * es, Tp * H * es,       // sh_dab sh_dx
+      E * 4, E * 4,                        // order ret_order
   };
   L.n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   size_t off = 0;
@@ -120,7 +121,7 @@ const char* const kEntryNames[] = {
     "tile_off", "rowp_of_pair", "row_of_pair", "pair_of_row", "x_perm", "ab", "h", "y_pair", "sh_ab", "sh_h",
     "sh_y", "g", "score", "dy_perm", "ret_cidx", "ret_count", "ret_offset", "ret_pad_off", "ret_tile_off",
     "ret_src", "crow_of_pair", "ret_rows", "x_c", "ab_c", "h_c", "dy_c", "dab", "dx_pair", "dl", "dl_sel", "wrT",
-    "sh_dab", "sh_dx"};
+    "sh_dab", "sh_dx", "order", "ret_order"};
 
 WsPtrs make_ptrs(const WsLayout& L, void* ws) {
   char* b = static_cast<char*>(ws);
@@ -170,6 +171,8 @@ WsPtrs make_ptrs(const WsLayout& L, void* ws) {
   p.wrT = nx();
   p.sh_dab = nx();
   p.sh_dx = nx();
+  p.order = (int*)nx();
+  p.ret_order = (int*)nx();
   return p;
 }
 
@@ -416,7 +419,7 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     Span sp(st, FAM_BW);
     CKL(launch_route_topk(p.logits, router_bias, T, E, k, p.topk_idx, p.topk_w, p.masks, st));
     CKL(launch_route_scan(p.masks, (int)L.C, E, p.count, p.offset, p.pad_off, p.tile_off, p.chunk_base, p.pair_of_row,
-                         expert_offsets, st));
+                         expert_offsets, st, p.order));
     CKL(launch_route_index(p.masks, p.chunk_base, p.topk_idx, p.offset, p.pad_off, T, E, k, p.rowp_of_pair,
                           p.row_of_pair, p.pair_of_row, st));
     if (bf)
@@ -448,6 +451,7 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.out1 = p.h;
     a.ldo1 = F;
     a.zero_pad = 1;
+    a.out_rows = L.Rmax;
     CKL(run_gemm(a, bf, 256, st, sms));
   }
   // expert down
@@ -469,6 +473,8 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.epi = EPI_STORE;
     a.out0 = p.y_pair;
     a.ldo = H;
+    a.zero_pad = 1;
+    a.out_rows = L.Rmax;
     CKL(run_gemm(a, bf, 256, st, sms));
   }
   if (shared) {
@@ -492,6 +498,7 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.out1 = p.sh_h;
     a.ldo1 = Fs;
     a.zero_pad = 1;
+    a.out_rows = L.Tpad;
     CKL(run_gemm(a, bf, 256, st, sms));
     GemmArgs b = base_args(p.status);
     b.var_k = 0;
@@ -508,6 +515,8 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     b.epi = EPI_STORE;
     b.out0 = p.sh_y;
     b.ldo = H;
+    b.zero_pad = 1;
+    b.out_rows = L.Tpad;
     CKL(run_gemm(b, bf, 256, st, sms));
   }
   {
@@ -571,7 +580,8 @@ int moe_select_retained(const moe_dims* dims, void* ws, size_t ws_bytes, void* s
       CKL(launch_pair_score<float>(dy, p.y_pair, p.pair_of_row, p.pad_off + E, L.Rmax, p.topk_w, p.xnorm, H, k, p.g,
                                   p.score, nullptr, scores, sms, st));
     CKL(launch_select(p.score, p.count, p.pad_off, quota, E, p.ret_cidx, p.ret_count, p.status, st));
-    CKL(launch_ret_scan(p.ret_count, E, p.ret_offset, p.ret_pad_off, p.ret_tile_off, p.ret_src, retained_offsets, st));
+    CKL(launch_ret_scan(p.ret_count, E, p.ret_offset, p.ret_pad_off, p.ret_tile_off, p.ret_src, retained_offsets, st,
+                        p.ret_order));
     CKL(launch_ret_index(p.topk_idx, p.rowp_of_pair, p.row_of_pair, p.ret_cidx, p.ret_offset, p.ret_pad_off, L.P,
                         p.ret_src, p.crow_of_pair, p.ret_rows, retained_rows, sms, st));
     if (bf)
@@ -683,6 +693,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.out0 = p.dab;
     a.ldo = 2 * F;
     a.zero_pad = 1;
+    a.out_rows = L.Rmax;
     CKL(run_gemm(a, bf, 256, st, sms));
   }
   // dx_pair = [da | db] [W_gate ; W_up]^T
@@ -707,6 +718,8 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.epi = EPI_STORE;
     a.out0 = p.dx_pair;
     a.ldo = H;
+    a.zero_pad = 1;
+    a.out_rows = L.Rmax;
     CKL(run_gemm(a, bf, 256, st, sms));
   }
   if (shared) {
@@ -729,6 +742,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.out0 = p.sh_dab;
     a.ldo = 2 * Fs;
     a.zero_pad = 1;
+    a.out_rows = L.Tpad;
     CKL(run_gemm(a, bf, 256, st, sms));
     GemmArgs b = base_args(p.status);
     b.var_k = 0;
@@ -748,6 +762,8 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     b.epi = EPI_STORE;
     b.out0 = p.sh_dx;
     b.ldo = H;
+    b.zero_pad = 1;
+    b.out_rows = L.Tpad;
     CKL(run_gemm(b, bf, 256, st, sms));
   }
   {
@@ -790,6 +806,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
       a.out1 = dw_up;
       a.ldo = F;
       a.out_gstride = L.H * L.F;
+      a.g_order = use_retained ? p.ret_order : p.order;
       CKL(run_gemm(a, bf, 256, st, sms));
     }
     // dW_down[e] = h_e^T dy_e
@@ -811,6 +828,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
       a.out0 = dw_down;
       a.ldo = H;
       a.out_gstride = L.F * L.H;
+      a.g_order = use_retained ? p.ret_order : p.order;
       CKL(run_gemm(a, bf, 256, st, sms));
     }
     // dW_router = x^T dl

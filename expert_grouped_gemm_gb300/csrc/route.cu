@@ -79,11 +79,12 @@ __global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* 
 // One block of 1024 threads, thread e = expert e.
 __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset,
                                                      int* pad_off, int* tile_off, int* chunk_base, int* pair_of_row,
-                                                     int* user_offsets) {
+                                                     int* user_offsets, int* order) {
   const int e = threadIdx.x;
   int cnt = 0;
   if (e < E)
     for (int c = 0; c < C; ++c) cnt += __popcll(masks[(int64_t)c * E + e]);
+  if (order) block_order_desc(cnt, E, order);
   const int pad = (cnt + 15) / 16 * 16;
   const int tiles = (cnt + 127) / 128;
   int tot_c, tot_p, tot_t;
@@ -236,9 +237,10 @@ cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, in
 }
 
 cudaError_t launch_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset, int* pad_off,
-                              int* tile_off, int* chunk_base, int* pair_of_row, int* user_offsets, cudaStream_t st) {
+                              int* tile_off, int* chunk_base, int* pair_of_row, int* user_offsets, cudaStream_t st,
+                              int* order) {
   k_route_scan<<<1, 1024, 0, st>>>(masks, C, E, count, offset, pad_off, tile_off, chunk_base, pair_of_row,
-                                   user_offsets);
+                                   user_offsets, order);
   return cudaGetLastError();
 }
 
