@@ -299,10 +299,12 @@ __global__ void k_transpose(const TIO* in, int R, int Cc, TIO* out) {
 
 // ------------------------------------------------------------------ dX reduce
 // Warp per token: dX_t = sum_j [kept] dx_pair[crow(t,j)] + sum_j dl_j W_r[:,e_j] (+ shared dX_t).
+// Rows of up to 8 slots are loaded together before they are summed (slot order kept).
 template <typename TIO>
-__global__ void __launch_bounds__(256) k_dx_reduce(const TIO* dx_pair, const int* crow_of_pair, const int* topk_idx,
-                                                   const float* dl_sel, const TIO* wrT, const TIO* sh_dx, int T, int H,
-                                                   int k, TIO* dx) {
+__global__ void __launch_bounds__(256) k_dx_reduce(const TIO* __restrict__ dx_pair, const int* __restrict__ crow_of_pair,
+                                                   const int* __restrict__ topk_idx, const float* __restrict__ dl_sel,
+                                                   const TIO* __restrict__ wrT, const TIO* __restrict__ sh_dx, int T,
+                                                   int H, int k, TIO* __restrict__ dx) {
   const int lane = threadIdx.x & 31;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
     const int64_t p0 = (int64_t)t * k;
@@ -310,18 +312,37 @@ __global__ void __launch_bounds__(256) k_dx_reduce(const TIO* dx_pair, const int
     if constexpr (sizeof(TIO) == 2) {
       for (int i = lane; i < H / 8; i += 32) {
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, f[8];
-        for (int j = 0; j < k; ++j) {
-          const int cr = crow_of_pair[p0 + j];
-          if (cr < 0) continue;
-          bf16x8_to_f(reinterpret_cast<const uint4*>(dx_pair + (int64_t)cr * H)[i], f);
+        for (int j0 = 0; j0 < k; j0 += 8) {
+          uint4 u[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] += f[q];
+          for (int jj = 0; jj < 8; ++jj) {
+            u[jj] = make_uint4(0, 0, 0, 0);
+            const int cr = (j0 + jj < k) ? crow_of_pair[p0 + j0 + jj] : -1;
+            if (cr >= 0) u[jj] = reinterpret_cast<const uint4*>(dx_pair + (int64_t)cr * H)[i];
+          }
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            if (j0 + jj < k && crow_of_pair[p0 + j0 + jj] >= 0) {
+              bf16x8_to_f(u[jj], f);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) acc[q] += f[q];
+            }
+          }
         }
-        for (int j = 0; j < k; ++j) {
-          const float d = dl_sel[p0 + j];
-          bf16x8_to_f(reinterpret_cast<const uint4*>(wrT + (int64_t)topk_idx[p0 + j] * H)[i], f);
+        for (int j0 = 0; j0 < k; j0 += 8) {
+          uint4 u[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] = fmaf(d, f[q], acc[q]);
+          for (int jj = 0; jj < 8; ++jj)
+            if (j0 + jj < k) u[jj] = reinterpret_cast<const uint4*>(wrT + (int64_t)topk_idx[p0 + j0 + jj] * H)[i];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            if (j0 + jj < k) {
+              const float d = dl_sel[p0 + j0 + jj];
+              bf16x8_to_f(u[jj], f);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) acc[q] = fmaf(d, f[q], acc[q]);
+            }
+          }
         }
         if (sh_dx) {
           bf16x8_to_f(reinterpret_cast<const uint4*>(sh_dx + (int64_t)t * H)[i], f);

@@ -122,7 +122,7 @@ __device__ __forceinline__ void aux_prefetch(uint32_t buf, const __nv_bfloat16* 
   cp_async_commit();
 }
 
-template <int BN, int STAGES, int EPI_WARP_BYTES>
+template <int BN, int STAGES, int EPI_WARP_BYTES, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
@@ -287,10 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     const int row = q * 32 + lane;
     const uint32_t wstage = smem_u32(smem + C::EPI_OFF + (warp - 2) * EPI_WARP_BYTES);
-    const bool tma_out = args.epi != EPI_F32;
-    const bool bwd = args.epi == EPI_SWIGLU_BWD;
-    const bool fwd = args.epi == EPI_SWIGLU_FWD;
-    const int nout = fwd ? 3 : ((bwd || (args.epi == EPI_DW && args.paired)) ? 2 : 1);
+    constexpr bool tma_out = EPI != EPI_F32;
+    constexpr bool bwd = EPI == EPI_SWIGLU_BWD;
+    constexpr bool fwd = EPI == EPI_SWIGLU_FWD;
+    // staged outputs per chunk (the SwiGLU forward stages a|b, then h in the a tile)
+    const int nout = (fwd || bwd || (EPI == EPI_DW && args.paired)) ? 2 : 1;
     // one output alternates two staging sets when room allows; otherwise one set
     const int nbuf = (nout == 1 && EPI_WARP_BYTES >= 2 * kStageTileBytes) ? 2 : 1;
     const uint32_t aux_buf = wstage + 2 * kStageTileBytes;  // SwiGLU bwd: a and b tiles of one chunk
@@ -345,6 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           cp_async_wait<0>();
           __syncwarp();
         }
+        uint4 hpk[8];  // SwiGLU forward: h of this chunk, staged after a|b have been read
+#pragma unroll
         for (int hh = 0; hh < 2; ++hh) {  // two 32-column halves of the chunk
           if (!empty_tile) {
             tmem_ld32_async(taddr + c * 64 + hh * 32, ra);
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_ld_wait(ra);
             }
           }
-          if (!tma_out) {  // fp32 logits (single group): direct 16-byte stores, one row per thread
+          if constexpr (!tma_out) {  // fp32 logits (single group): direct 16-byte stores, one row per thread
             const int nh = n0 + hh * 32;
             if (!empty_tile && m < ti.rows && nh < args.N) {
               float* o = reinterpret_cast<float*>(args.out0) + ((int64_t)ti.off + m) * args.ldo + nh;
@@ -382,16 +385,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               x0[i] = live ? __uint_as_float(ra[8 * g8 + i]) : 0.0f;
               x1[i] = live ? __uint_as_float(rb[8 * g8 + i]) : 0.0f;
             }
-            if (fwd) {
+            if constexpr (fwd) {
               float h[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) h[i] = x0[i] * sigmoidf_(x0[i]) * x1[i];
+              hpk[j] = f_to_bf16x8(h);
               if (store) {
                 st_shared_v4(set + stage_off(lane, j), f_to_bf16x8(x0));
                 st_shared_v4(set + kStageTileBytes + stage_off(lane, j), f_to_bf16x8(x1));
-                st_shared_v4(set + 2 * kStageTileBytes + stage_off(lane, j), f_to_bf16x8(h));
               }
-            } else if (bwd) {
+            } else if constexpr (bwd) {
               float av[8], bv[8], da[8], db[8];
               bf16x8_to_f(ld_shared_v4(aux_buf + stage_off(lane, j)), av);
               bf16x8_to_f(ld_shared_v4(aux_buf + kStageTileBytes + stage_off(lane, j)), bv);
@@ -405,7 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st_shared_v4(set + stage_off(lane, j), f_to_bf16x8(da));
                 st_shared_v4(set + kStageTileBytes + stage_off(lane, j), f_to_bf16x8(db));
               }
-            } else if (store) {  // EPI_DW / EPI_STORE
+            } else {  // EPI_DW / EPI_STORE
+              if (!store) continue;
               st_shared_v4(set + stage_off(lane, j), f_to_bf16x8(x0));
               if (nout > 1) st_shared_v4(set + kStageTileBytes + stage_off(lane, j), f_to_bf16x8(x1));
             }
@@ -429,8 +433,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const CUtensorMap* o1 = ab_row ? o0 : (full_box ? &tmO1 : &tmO1h);
           tma_store_2d(o0, set, n0, (int)out_row0);
           if (nout > 1) tma_store_2d(o1, set + kStageTileBytes, c1, (int)out_row0);
-          if (nout > 2) tma_store_2d(full_box ? &tmO1 : &tmO1h, set + 2 * kStageTileBytes, n0, (int)out_row0);
           bulk_commit();
+        }
+        if (fwd) {  // h goes out through the a tile once a|b have been read from it
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) st_shared_v4(set + stage_off(lane, j), hpk[j]);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(rows_left >= 32 ? &tmO1 : &tmO1h, set, n0, (int)out_row0);
+            bulk_commit();
+          }
         }
       }
       if (!empty_tile) {
@@ -496,11 +511,12 @@ static bool make_map_mn3d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, int EPI_WARP_BYTES>
+template <int BN, int STAGES, int EPI_WARP_BYTES, int EPI>
 static cudaError_t launch_cfg(const GemmArgs& a, cudaStream_t st, int num_sms) {
   using C = TcCfg<BN, STAGES, EPI_WARP_BYTES>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
-  auto kern = tc_grouped_gemm<BN, STAGES, EPI_WARP_BYTES>;
+  if (a.epi != EPI) return cudaErrorInvalidValue;
+  auto kern = tc_grouped_gemm<BN, STAGES, EPI_WARP_BYTES, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   CUtensorMap mA, mB0, mB1, mO0, mO1, mO0h, mO1h;
@@ -539,29 +555,40 @@ static cudaError_t launch_cfg(const GemmArgs& a, cudaStream_t st, int num_sms) {
 }
 
 // Staging bytes one epilogue warp needs: nout 4 KB tiles (one output with room
-// for two alternates two sets), plus an a|b tile pair for the SwiGLU backward.
+// for two alternates two sets; the SwiGLU forward reuses its a tile for h),
+// plus an a|b tile pair for the SwiGLU backward.
 static int staging_bytes(const GemmArgs& a) {
   if (a.epi == EPI_F32) return 0;
-  if (a.epi == EPI_SWIGLU_FWD) return 3 * kStageTileBytes;
+  if (a.epi == EPI_SWIGLU_FWD) return 2 * kStageTileBytes;
   if (a.epi == EPI_SWIGLU_BWD) return 2 * kStageTileBytes + 2 * kStageTileBytes;
   return ((a.epi == EPI_DW && a.paired) ? 2 : 1) * kStageTileBytes;
 }
 
 cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_sms, int /*max_tiles_hint*/) {
   const int need = staging_bytes(a);
+  constexpr int kT = kStageTileBytes;
   if (bn == 128) {
-    constexpr int kEpi = kStageTileBytes;
-    if (a.epi == EPI_SWIGLU_BWD || a.epi == EPI_SWIGLU_FWD || need > kEpi) return cudaErrorInvalidValue;
-    return launch_cfg<128, 6, kEpi>(a, st, num_sms);
+    if (need > kT) return cudaErrorInvalidValue;
+    if (a.epi == EPI_F32) return launch_cfg<128, 6, kT, EPI_F32>(a, st, num_sms);
+    if (a.epi == EPI_DW) return launch_cfg<128, 6, kT, EPI_DW>(a, st, num_sms);
+    return cudaErrorInvalidValue;
   }
-  if (a.epi == EPI_SWIGLU_BWD || a.epi == EPI_SWIGLU_FWD) {
-    constexpr int kEpi = 4 * kStageTileBytes;
-    if (need > kEpi) return cudaErrorInvalidValue;
-    return launch_cfg<256, 3, kEpi>(a, st, num_sms);
+  switch (a.epi) {
+    case EPI_SWIGLU_BWD:
+      if (need > 4 * kT) return cudaErrorInvalidValue;
+      return launch_cfg<256, 3, 4 * kT, EPI_SWIGLU_BWD>(a, st, num_sms);
+    case EPI_SWIGLU_FWD:
+      if (need > 2 * kT) return cudaErrorInvalidValue;
+      return launch_cfg<256, 4, 2 * kT, EPI_SWIGLU_FWD>(a, st, num_sms);
+    case EPI_STORE:
+      if (need > 2 * kT) return cudaErrorInvalidValue;
+      return launch_cfg<256, 4, 2 * kT, EPI_STORE>(a, st, num_sms);
+    case EPI_DW:
+      if (need > 2 * kT) return cudaErrorInvalidValue;
+      return launch_cfg<256, 4, 2 * kT, EPI_DW>(a, st, num_sms);
+    default:
+      return cudaErrorInvalidValue;
   }
-  constexpr int kEpi = 2 * kStageTileBytes;
-  if (need > kEpi) return cudaErrorInvalidValue;
-  return launch_cfg<256, 4, kEpi>(a, st, num_sms);
 }
 
 }  // namespace moe

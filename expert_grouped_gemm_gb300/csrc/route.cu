@@ -19,31 +19,43 @@ namespace moe {
 constexpr int kChunk = 64;  // tokens per routing chunk (one bit each in a uint64 mask)
 
 // ------------------------------------------------------------------ top-k
-// grid = C chunks, block = 256 (8 warps); warp per token.
-__global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* bias, int T, int E, int k,
-                                                    int* topk_idx, float* topk_w, uint64_t* masks) {
+// grid = C chunks of 64 tokens, block = 1024 (32 warps, two tokens each).
+// Warp per token; lane l holds logits e = l + 32 i (i < EPL) in registers.
+template <int EPL>
+__global__ void __launch_bounds__(1024) k_route_topk(float* logits, const float* bias, int T, int E, int k,
+                                                     int* topk_idx, float* topk_w, uint64_t* masks) {
   extern __shared__ uint64_t smask[];  // [E]
   const int c = blockIdx.x;
   for (int e = threadIdx.x; e < E; e += blockDim.x) smask[e] = 0ull;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int tl = warp; tl < kChunk; tl += 8) {
+  for (int tl = warp; tl < kChunk; tl += 32) {
     const int t = c * kChunk + tl;
     if (t >= T) break;
     float* lrow = logits + (int64_t)t * E;
-    for (int e = lane; e < E; e += 32) lrow[e] = lrow[e] + (bias ? bias[e] : 0.0f);
-    __syncwarp();
-    uint32_t taken = 0;  // bit i: expert lane + 32 i already selected
+    float v[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        const float x = lrow[e] + (bias ? bias[e] : 0.0f);
+        lrow[e] = x;                     // the biased logits the selection used
+        v[i] = (x != x) ? -INFINITY : x;  // NaN ranks last
+      }
+    }
+    uint32_t taken = 0;  // bit i: expert lane + 32 i already selected (or absent)
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i >= E) taken |= 1u << i;
     float lmax = 0.0f, sum = 0.0f;
     for (int j = 0; j < k; ++j) {
       float bv = -INFINITY;
       int be = 0x7fffffff;
-      for (int i = 0, e = lane; e < E; ++i, e += 32) {
-        if ((taken >> i) & 1u) continue;
-        float v = lrow[e];
-        if (v != v) v = -INFINITY;  // NaN ranks last
-        if (be == 0x7fffffff || v > bv || (v == bv && e < be)) {
-          bv = v;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (!((taken >> i) & 1u) && (be == 0x7fffffff || v[i] > bv)) {  // e ascending: ties keep the first
+          bv = v[i];
           be = e;
         }
       }
@@ -187,23 +199,34 @@ __global__ void __launch_bounds__(256) k_gather_rows(const TIO* x, const int* pa
 
 // ------------------------------------------------------------------ combine
 // Warp per token: y[t] = sum_j w[t,j] y_pair[row(t,j)] (+ shared y[t]), slots ascending.
+// The rows of up to 8 slots are loaded together before they are summed.
 template <typename TIO>
-__global__ void __launch_bounds__(256) k_combine(const TIO* y_pair, const int* rowp_of_pair, const float* topk_w,
-                                                 const TIO* sh_y, int T, int H, int k, TIO* y) {
+__global__ void __launch_bounds__(256) k_combine(const TIO* __restrict__ y_pair, const int* __restrict__ rowp_of_pair,
+                                                 const float* __restrict__ topk_w, const TIO* __restrict__ sh_y, int T,
+                                                 int H, int k, TIO* __restrict__ y) {
   const int lane = threadIdx.x & 31;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
     TIO* dst = y + (int64_t)t * H;
+    const int64_t p0 = (int64_t)t * k;
     if constexpr (sizeof(TIO) == 2) {
       const int nv = H / 8;
       for (int i = lane; i < nv; i += 32) {
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int j = 0; j < k; ++j) {
-          const float w = topk_w[(int64_t)t * k + j];
-          const int r = rowp_of_pair[(int64_t)t * k + j];
-          float f[8];
-          bf16x8_to_f(reinterpret_cast<const uint4*>(y_pair + (int64_t)r * H)[i], f);
+        for (int j0 = 0; j0 < k; j0 += 8) {
+          uint4 u[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] = fmaf(w, f[q], acc[q]);
+          for (int jj = 0; jj < 8; ++jj)
+            if (j0 + jj < k) u[jj] = reinterpret_cast<const uint4*>(y_pair + (int64_t)rowp_of_pair[p0 + j0 + jj] * H)[i];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            if (j0 + jj < k) {
+              const float w = topk_w[p0 + j0 + jj];
+              float f[8];
+              bf16x8_to_f(u[jj], f);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) acc[q] = fmaf(w, f[q], acc[q]);
+            }
+          }
         }
         if (sh_y) {
           float f[8];
@@ -217,8 +240,8 @@ __global__ void __launch_bounds__(256) k_combine(const TIO* y_pair, const int* r
       for (int i = lane; i < H; i += 32) {
         float acc = 0.0f;
         for (int j = 0; j < k; ++j) {
-          const float w = topk_w[(int64_t)t * k + j];
-          const int r = rowp_of_pair[(int64_t)t * k + j];
+          const float w = topk_w[p0 + j];
+          const int r = rowp_of_pair[p0 + j];
           acc = fmaf(w, io<TIO>::to_f(y_pair[(int64_t)r * H + i]), acc);
         }
         if (sh_y) acc += io<TIO>::to_f(sh_y[(int64_t)t * H + i]);
@@ -232,7 +255,14 @@ __global__ void __launch_bounds__(256) k_combine(const TIO* y_pair, const int* r
 cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, int k, int* topk_idx, float* topk_w,
                               uint64_t* masks, cudaStream_t st) {
   const int C = (T + kChunk - 1) / kChunk;
-  k_route_topk<<<C, 256, E * sizeof(uint64_t), st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  const size_t sm = E * sizeof(uint64_t);
+  const int epl = (E + 31) / 32;
+  if (epl <= 1) k_route_topk<1><<<C, 1024, sm, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  else if (epl <= 2) k_route_topk<2><<<C, 1024, sm, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  else if (epl <= 4) k_route_topk<4><<<C, 1024, sm, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  else if (epl <= 8) k_route_topk<8><<<C, 1024, sm, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  else if (epl <= 16) k_route_topk<16><<<C, 1024, sm, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  else k_route_topk<32><<<C, 1024, sm, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
   return cudaGetLastError();
 }
 
