@@ -147,16 +147,21 @@ __global__ void __launch_bounds__(256) k_select(const float* score, const int* c
 
 // One block of 1024 threads: offsets of the kept rows, exact and padded.
 __global__ void __launch_bounds__(1024) k_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off,
-                                                   int* ret_tile_off, int* ret_src, int* user_offsets, int* order) {
+                                                   int* ret_tile_off, int* ret_src, int* user_offsets, int* order,
+                                                   int* ret_tile_off2) {
   const int e = threadIdx.x;
   const int cnt = e < E ? ret_count[e] : 0;
   if (order) block_order_desc(cnt, E, order);
   const int pad = (cnt + 15) / 16 * 16;
   const int tiles = (cnt + 127) / 128;
-  int tc, tp, tt;
+  const int tiles2 = (cnt + 255) / 256;
+  int tc, tp, tt, tt2;
   const int oc = block_excl_scan(cnt, &tc);
   const int op = block_excl_scan(pad, &tp);
   const int ot = block_excl_scan(tiles, &tt);
+  const int ot2 = block_excl_scan(tiles2, &tt2);
+  if (ret_tile_off2 && e < E) ret_tile_off2[e] = ot2;
+  if (ret_tile_off2 && e == 0) ret_tile_off2[E] = tt2;
   if (e < E) {
     ret_offset[e] = oc;
     ret_pad_off[e] = op;
@@ -390,8 +395,9 @@ cudaError_t launch_select(const float* score, const int* count, const int* pad_o
 }
 
 cudaError_t launch_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off, int* ret_tile_off,
-                            int* ret_src, int* user_offsets, cudaStream_t st, int* order) {
-  k_ret_scan<<<1, 1024, 0, st>>>(ret_count, E, ret_offset, ret_pad_off, ret_tile_off, ret_src, user_offsets, order);
+                            int* ret_src, int* user_offsets, cudaStream_t st, int* order, int* ret_tile_off2) {
+  k_ret_scan<<<1, 1024, 0, st>>>(ret_count, E, ret_offset, ret_pad_off, ret_tile_off, ret_src, user_offsets, order,
+                                 ret_tile_off2);
   return cudaGetLastError();
 }
 

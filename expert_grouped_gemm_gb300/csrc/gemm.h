@@ -33,6 +33,7 @@ struct GemmArgs {
   const int* rows;      // [G] rows per group, or null: single group of rows_const rows
   const int* row_off;   // [G+1] padded row offsets (prefix), or null: 0
   const int* tile_off;  // [G+1] prefix of ceil(rows/128) per group (var-M), or null (single group)
+  const int* tile_off2; // [G+1] prefix of ceil(rows/256) per group (var-M, two-CTA tiles), or null
   int rows_const;
   int M;                // var-K: output rows
   int N;                // output columns (per half when paired)

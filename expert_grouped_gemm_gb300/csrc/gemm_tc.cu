@@ -32,11 +32,12 @@ constexpr int kThreads = 192;
 constexpr int kStageRowBytes = 128;                   // 64 bf16 per staged row
 constexpr int kStageTileBytes = 32 * kStageRowBytes;  // one warp's 32 rows x 64 columns (4 KB)
 
-template <int BN, int STAGES, int EPI_WARP_BYTES>
+template <int BN, int STAGES, int EPI_WARP_BYTES, int CTAS>
 struct TcCfg {
-  static constexpr int A_BYTES = kTileM * kTileK * 2;  // 16 KB
-  static constexpr int B_BYTES = BN * kTileK * 2;      // 32 KB (BN=256) / 16 KB
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int A_BYTES = kTileM * kTileK * 2;       // 16 KB: this CTA's 128 rows
+  static constexpr int B_BYTES = BN * kTileK * 2 / CTAS;    // this CTA's share of the BN columns
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // per CTA
+  static constexpr int TILE_M = kTileM * CTAS;              // rows of one (pair) tile
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + 4 * EPI_WARP_BYTES;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;  // barriers + 1 KB alignment slack
@@ -54,15 +55,16 @@ __device__ __forceinline__ int n_tiles(const GemmArgs& a) {
   return (a.N + w - 1) / w;
 }
 
-template <int BN>
+template <int BN, int TILE_M>
 __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int NT) {
   TileInfo ti;
+  const int* toff = TILE_M == kTileM ? a.tile_off : a.tile_off2;
   if (a.var_k) {
-    const int MT = (a.M + kTileM - 1) / kTileM;
+    const int MT = (a.M + TILE_M - 1) / TILE_M;
     const int gi = t / (MT * NT);
     const int rem = t - gi * MT * NT;
     ti.g = a.g_order ? a.g_order[gi] : gi;
-    ti.m0 = (rem / NT) * kTileM;
+    ti.m0 = (rem / NT) * TILE_M;
     ti.nt = rem % NT;
     ti.rows = grp_rows(a, ti.g);
     ti.off = grp_off(a, ti.g);
@@ -71,16 +73,16 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int NT
     const int u = t / NT;
     ti.nt = t - u * NT;
     int g = 0;
-    if (a.tile_off) {  // last g with tile_off[g] <= u
+    if (toff) {  // last g with toff[g] <= u
       int lo = 0, hi = a.G - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (a.tile_off[mid] <= u) lo = mid; else hi = mid - 1;
+        if (toff[mid] <= u) lo = mid; else hi = mid - 1;
       }
       g = lo;
-      ti.m0 = (u - a.tile_off[g]) * kTileM;
+      ti.m0 = (u - toff[g]) * TILE_M;
     } else {
-      ti.m0 = u * kTileM;
+      ti.m0 = u * TILE_M;
     }
     ti.g = g;
     ti.rows = grp_rows(a, g);
@@ -90,11 +92,12 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int NT
   return ti;
 }
 
-template <int BN>
+template <int BN, int TILE_M>
 __device__ __forceinline__ int total_tiles(const GemmArgs& a) {
   const int NT = n_tiles<BN>(a);
-  if (a.var_k) return a.G * ((a.M + kTileM - 1) / kTileM) * NT;
-  const int mt = a.tile_off ? a.tile_off[a.G] : (a.rows_const + kTileM - 1) / kTileM;
+  const int* toff = TILE_M == kTileM ? a.tile_off : a.tile_off2;
+  if (a.var_k) return a.G * ((a.M + TILE_M - 1) / TILE_M) * NT;
+  const int mt = toff ? toff[a.G] : (a.rows_const + TILE_M - 1) / TILE_M;
   return mt * NT;
 }
 
@@ -122,13 +125,14 @@ __device__ __forceinline__ void aux_prefetch(uint32_t buf, const __nv_bfloat16* 
   cp_async_commit();
 }
 
-template <int BN, int STAGES, int EPI_WARP_BYTES, int EPI>
+template <int BN, int STAGES, int EPI_WARP_BYTES, int EPI, int CTAS>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
                     const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO0h,
                     const __grid_constant__ CUtensorMap tmO1h, const GemmArgs args) {
-  using C = TcCfg<BN, STAGES, EPI_WARP_BYTES>;
+  using C = TcCfg<BN, STAGES, EPI_WARP_BYTES, CTAS>;
+  constexpr bool PAIR = CTAS == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -141,28 +145,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // In a CTA pair, rank 0 (the leader) issues the MMAs for both CTAs; each CTA
+  // loads its own 128 rows of A and its half of the B columns, and its tensor
+  // memory receives its own 128 rows of the accumulator.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int cluster_id = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int num_clusters = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&full[s], 1);   // the leader's producer arms it for both CTAs' bytes
+      mbar_init(&empty[s], 1);  // one MMA commit (multicast to both CTAs of a pair)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 128);
+      mbar_init(&tempty[i], 4 * CTAS);  // one arrive per epilogue warp of each CTA
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 2) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  if (warp == 2) {
+    if constexpr (PAIR) tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+    else tmem_alloc(tmem_slot, C::TMEM_COLS);
+  }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // leader barriers as seen from this CTA (shared::cluster addresses)
+  const uint32_t full0 = PAIR ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
+  const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
 
   const int NT = n_tiles<BN>(args);
-  const int total = total_tiles<BN>(args);
+  const int total = total_tiles<BN, C::TILE_M>(args);
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
@@ -175,8 +193,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const TileInfo ti = decode_tile<BN>(args, t, NT);
+    auto load2 = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+      if constexpr (PAIR) tma_load_2d_pair(dst, map, bar, c0, c1);
+      else tma_load_2d(dst, map, bar, c0, c1);
+    };
+    auto load3 = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1, int c2) {
+      if constexpr (PAIR) tma_load_3d_pair(dst, map, bar, c0, c1, c2);
+      else tma_load_3d(dst, map, bar, c0, c1, c2);
+    };
+    for (int t = cluster_id; t < total && ok; t += num_clusters) {
+      const TileInfo ti = decode_tile<BN, C::TILE_M>(args, t, NT);
+      const int m0c = ti.m0 + (int)rank * kTileM;  // this CTA's rows (var-M) / columns (var-K) of A
       for (int kb = 0; kb < ti.kblocks; ++kb) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
           ok = false;
@@ -184,31 +211,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* sa = smem + stage * C::STAGE_BYTES;
         uint8_t* sb = sa + C::A_BYTES;
-        const uint32_t fb = smem_u32(&full[stage]);
-        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+        const uint32_t fb = full0 + stage * 8;  // the leader's full barrier of this stage
+        if (leader) mbar_arrive_expect_tx(&full[stage], CTAS * C::STAGE_BYTES);
         issued_parity[stage] = (int)phase;
         // A
         if (!args.var_k) {
-          tma_load_2d(smem_u32(sa), &tmA, fb, kb * kTileK, ti.off + ti.m0);
+          load2(smem_u32(sa), &tmA, fb, kb * kTileK, ti.off + m0c);
         } else if (C::MN3D) {
-          tma_load_3d(smem_u32(sa), &tmA, fb, 0, ti.off + kb * kTileK, ti.m0 / 64);
+          load3(smem_u32(sa), &tmA, fb, 0, ti.off + kb * kTileK, m0c / 64);
         } else {
-          tma_load_2d(smem_u32(sa), &tmA, fb, ti.m0, ti.off + kb * kTileK);
-          tma_load_2d(smem_u32(sa + 8192), &tmA, fb, ti.m0 + 64, ti.off + kb * kTileK);
+          load2(smem_u32(sa), &tmA, fb, m0c, ti.off + kb * kTileK);
+          load2(smem_u32(sa + 8192), &tmA, fb, m0c + 64, ti.off + kb * kTileK);
         }
-        // B
+        // B (a pair splits the BN columns: rank 0 the first half, rank 1 the second)
         if (args.b_kmajor) {
           const bool second = args.k_split > 0 && kb * kTileK >= args.k_split;
           const int kk = second ? kb - args.k_split / kTileK : kb;
-          tma_load_2d(smem_u32(sb), second ? &tmB1 : &tmB0, fb, kk * kTileK, ti.g * args.N + ti.nt * BN);
+          load2(smem_u32(sb), second ? &tmB1 : &tmB0, fb, kk * kTileK,
+                ti.g * args.N + ti.nt * BN + (int)rank * (BN / CTAS));
         } else {
           const int brow = args.var_k ? ti.off + kb * kTileK : ti.g * args.K + kb * kTileK;
           if (C::MN3D) {
-            if (args.paired) {  // two halves of BN/2 columns: B0 then B1 (at column offset b1_col)
-              tma_load_3d(smem_u32(sb), &tmB0, fb, 0, brow, ti.nt * (BN / 128));
-              tma_load_3d(smem_u32(sb + BN / 2 * 128), &tmB1, fb, 0, brow, args.b1_col / 64 + ti.nt * (BN / 128));
+            if (args.paired) {  // halves of BN/2 columns: B0, then B1 at column offset b1_col
+              if (!PAIR || rank == 0) load3(smem_u32(sb), &tmB0, fb, 0, brow, ti.nt * (BN / 128));
+              if (!PAIR || rank == 1)
+                load3(smem_u32(PAIR ? sb : sb + BN / 2 * 128), &tmB1, fb, 0, brow,
+                      args.b1_col / 64 + ti.nt * (BN / 128));
             } else {
-              tma_load_3d(smem_u32(sb), &tmB0, fb, 0, brow, ti.nt * (BN / 64));
+              load3(smem_u32(sb), &tmB0, fb, 0, brow, ti.nt * (BN / 64) + (int)rank * (BN / 64 / CTAS));
             }
           } else {
 #pragma unroll
@@ -225,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               } else {
                 col = ti.nt * BN + c * 64;
               }
-              tma_load_2d(smem_u32(sb + c * 8192), map, fb, col, brow);
+              load2(smem_u32(sb + c * 8192), map, fb, col, brow);
             }
           }
         }
@@ -235,22 +265,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // make sure no copy of ours is still landing in shared memory
-    for (int s = 0; s < STAGES; ++s)
-      if (issued_parity[s] >= 0) mbar_wait_timed(&full[s], (uint32_t)issued_parity[s], 200000000ull);
-  } else if (warp == 1 && lane == 0) {
+    // make sure no copy of ours is still landing in shared memory (the leader's
+    // full barriers also count the peer's bytes)
+    if (leader)
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_parity[s] >= 0) mbar_wait_timed(&full[s], (uint32_t)issued_parity[s], 200000000ull);
+  } else if (warp == 1 && lane == 0 && leader) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = idesc_bf16(kTileM, BN, args.var_k, args.b_kmajor ? 0 : 1);
+    const uint32_t idesc = idesc_bf16(C::TILE_M, BN, args.var_k, args.b_kmajor ? 0 : 1);
     int stage = 0;
     uint32_t phase = 0;
     int acc_i = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const TileInfo ti = decode_tile<BN>(args, t, NT);
+    for (int t = cluster_id; t < total && ok; t += num_clusters) {
+      const TileInfo ti = decode_tile<BN, C::TILE_M>(args, t, NT);
       if (ti.kblocks == 0) continue;
       const int acc = acc_i & 1;
       const uint32_t acc_par = (uint32_t)((acc_i >> 1) & 1);
-      if (!mbar_wait_bounded(&tempty[acc], acc_par ^ 1u, abort_flag)) break;
+      const bool free_acc = PAIR ? mbar_wait_bounded_cluster(&tempty[acc], acc_par ^ 1u, abort_flag)
+                                 : mbar_wait_bounded(&tempty[acc], acc_par ^ 1u, abort_flag);
+      if (!free_acc) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       for (int kb = 0; kb < ti.kblocks; ++kb) {
@@ -267,20 +301,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t ad = args.var_k ? sdesc_sw128(sa + kk * 2048, 8192, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
           const uint64_t bd =
               args.b_kmajor ? sdesc_sw128(sb + kk * 32, 16, 1024) : sdesc_sw128(sb + kk * 2048, 8192, 1024);
-          tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          if constexpr (PAIR) tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          else tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
         }
-        tc_commit(&empty[stage]);
+        if constexpr (PAIR) tc_commit_pair_mc(&empty[stage]);
+        else tc_commit(&empty[stage]);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      tc_commit(&tfull[acc]);
+      if constexpr (PAIR) tc_commit_pair_mc(&tfull[acc]);
+      else tc_commit(&tfull[acc]);
       ++acc_i;
     }
     // wait until every MMA issued by this thread has completed
-    tc_commit(drain);
+    if constexpr (PAIR) tc_commit_pair(drain);
+    else tc_commit(drain);
     mbar_wait_timed(drain, 0, 200000000ull);
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
@@ -303,8 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ra[32], rb[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) rb[i] = 0u;  // only paired modes load it
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile<BN>(args, t, NT);
+    for (int t = cluster_id; t < total; t += num_clusters) {
+      TileInfo ti = decode_tile<BN, C::TILE_M>(args, t, NT);
+      ti.m0 += (int)rank * kTileM;  // this CTA's 128 rows of the (pair) tile
       const int m = ti.m0 + row;
       const int ncol0 = ti.nt * W;
       // rows of this tile that may be written, and the output row of this warp's box
@@ -448,9 +487,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!empty_tile) {
+      if (!empty_tile) {  // this warp is done with the accumulator: tell the MMA issuer
         tc_fence_before();
-        mbar_arrive(&tempty[acc]);
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR) mbar_arrive_cluster(tempty0 + acc * 8);
+          else mbar_arrive(&tempty[acc]);
+        }
         ++acc_i;
       }
     }
@@ -458,11 +501,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
 
+  tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // no CTA of the pair leaves while the other still uses it
+  tc_fence_after();
   if (threadIdx.x == 0 && *abort_flag) set_status(args.status, MOE_ERR_TIMEOUT);
   if (warp == 2) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -511,12 +557,13 @@ static bool make_map_mn3d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, int EPI_WARP_BYTES, int EPI>
+template <int BN, int STAGES, int EPI_WARP_BYTES, int EPI, int CTAS>
 static cudaError_t launch_cfg(const GemmArgs& a, cudaStream_t st, int num_sms) {
-  using C = TcCfg<BN, STAGES, EPI_WARP_BYTES>;
+  using C = TcCfg<BN, STAGES, EPI_WARP_BYTES, CTAS>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
+  static_assert(CTAS == 1 || BN == 256, "CTA pairs use the 256-column tile");
   if (a.epi != EPI) return cudaErrorInvalidValue;
-  auto kern = tc_grouped_gemm<BN, STAGES, EPI_WARP_BYTES, EPI>;
+  auto kern = tc_grouped_gemm<BN, STAGES, EPI_WARP_BYTES, EPI, CTAS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   CUtensorMap mA, mB0, mB1, mO0, mO1, mO0h, mO1h;
@@ -528,11 +575,11 @@ static cudaError_t launch_cfg(const GemmArgs& a, cudaStream_t st, int num_sms) {
   else
     ok = make_map_2d(&mA, a.A, a.a_rows, a.lda, 64, kTileK);
   const void* b1 = a.B1 ? a.B1 : a.B0;
-  if (a.b_kmajor) {
-    ok = ok && make_map_2d(&mB0, a.B0, a.b_rows, a.ldb, 64, BN);
-    ok = ok && make_map_2d(&mB1, b1, a.b_rows, a.ldb, 64, BN);
-  } else if (C::MN3D) {
-    const int chunks = a.paired ? BN / 128 : BN / 64;
+  if (a.b_kmajor) {  // each CTA loads BN/CTAS rows of B
+    ok = ok && make_map_2d(&mB0, a.B0, a.b_rows, a.ldb, 64, BN / CTAS);
+    ok = ok && make_map_2d(&mB1, b1, a.b_rows, a.ldb, 64, BN / CTAS);
+  } else if (C::MN3D) {  // each CTA loads BN/CTAS columns of B (paired: one half each)
+    const int chunks = (a.paired && CTAS == 1) ? BN / 128 : BN / 64 / CTAS;
     ok = ok && make_map_mn3d(&mB0, a.B0, a.b_rows, a.ldb, kTileK, chunks);
     ok = ok && make_map_mn3d(&mB1, b1, a.b_rows, a.ldb, kTileK, chunks);
   } else {
@@ -550,8 +597,30 @@ static cudaError_t launch_cfg(const GemmArgs& a, cudaStream_t st, int num_sms) {
     ok = ok && make_map_2d(&mO1, o1, orows, ld1, 64, 32) && make_map_2d(&mO1h, o1, orows, ld1, 64, 16);
   }
   if (!ok) return cudaErrorInvalidValue;
-  kern<<<num_sms, kThreads, C::SMEM, st>>>(mA, mB0, mB1, mO0, mO1, mO0h, mO1h, a);
-  return cudaGetLastError();
+  if constexpr (CTAS == 1) {
+    kern<<<num_sms, kThreads, C::SMEM, st>>>(mA, mB0, mB1, mO0, mO1, mO0h, mO1h, a);
+    return cudaGetLastError();
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // as many CTA pairs as can be resident at once (persistent schedule)
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) == cudaSuccess && max_clusters > 0 &&
+        2 * max_clusters < (int)cfg.gridDim.x)
+      cfg.gridDim = dim3(2 * max_clusters);
+    e = cudaLaunchKernelEx(&cfg, kern, mA, mB0, mB1, mO0, mO1, mO0h, mO1h, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
 }
 
 // Staging bytes one epilogue warp needs: nout 4 KB tiles (one output with room
@@ -569,23 +638,24 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_s
   constexpr int kT = kStageTileBytes;
   if (bn == 128) {
     if (need > kT) return cudaErrorInvalidValue;
-    if (a.epi == EPI_F32) return launch_cfg<128, 6, kT, EPI_F32>(a, st, num_sms);
-    if (a.epi == EPI_DW) return launch_cfg<128, 6, kT, EPI_DW>(a, st, num_sms);
+    if (a.epi == EPI_F32) return launch_cfg<128, 6, kT, EPI_F32, 1>(a, st, num_sms);
+    if (a.epi == EPI_DW) return launch_cfg<128, 6, kT, EPI_DW, 1>(a, st, num_sms);
     return cudaErrorInvalidValue;
   }
+  // 256-column tiles (the CTA-pair variant, CTAS = 2, is kept but measured slower)
   switch (a.epi) {
     case EPI_SWIGLU_BWD:
       if (need > 4 * kT) return cudaErrorInvalidValue;
-      return launch_cfg<256, 3, 4 * kT, EPI_SWIGLU_BWD>(a, st, num_sms);
+      return launch_cfg<256, 3, 4 * kT, EPI_SWIGLU_BWD, 1>(a, st, num_sms);
     case EPI_SWIGLU_FWD:
       if (need > 2 * kT) return cudaErrorInvalidValue;
-      return launch_cfg<256, 4, 2 * kT, EPI_SWIGLU_FWD>(a, st, num_sms);
+      return launch_cfg<256, 4, 2 * kT, EPI_SWIGLU_FWD, 1>(a, st, num_sms);
     case EPI_STORE:
       if (need > 2 * kT) return cudaErrorInvalidValue;
-      return launch_cfg<256, 4, 2 * kT, EPI_STORE>(a, st, num_sms);
+      return launch_cfg<256, 4, 2 * kT, EPI_STORE, 1>(a, st, num_sms);
     case EPI_DW:
       if (need > 2 * kT) return cudaErrorInvalidValue;
-      return launch_cfg<256, 4, 2 * kT, EPI_DW>(a, st, num_sms);
+      return launch_cfg<256, 4, 2 * kT, EPI_DW, 1>(a, st, num_sms);
     default:
       return cudaErrorInvalidValue;
   }

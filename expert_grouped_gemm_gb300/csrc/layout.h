@@ -57,6 +57,8 @@ struct WsPtrs {
   void* sh_dx;          // [Tpad,H]
   int* order;           // [E] experts by count, descending (dW scheduling order)
   int* ret_order;       // [E] experts by kept count, descending
+  int* tile_off2;       // [E+1] prefix of ceil(count/256) (two-CTA tiles)
+  int* ret_tile_off2;   // [E+1] prefix of ceil(kept/256)
 };
 
 struct WsLayout {

@@ -104,6 +104,7 @@ WsLayout make_layout(const moe_dims* d) {
       Tp * E * es, T * k * 4, E * H * es,  // dl dl_sel wrT
       Tp * 2 * Fs * es, Tp * H * es,       // sh_dab sh_dx
       E * 4, E * 4,                        // order ret_order
+      (E + 1) * 4, (E + 1) * 4,            // tile_off2 ret_tile_off2
   };
   L.n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   size_t off = 0;
@@ -121,7 +122,7 @@ const char* const kEntryNames[] = {
     "tile_off", "rowp_of_pair", "row_of_pair", "pair_of_row", "x_perm", "ab", "h", "y_pair", "sh_ab", "sh_h",
     "sh_y", "g", "score", "dy_perm", "ret_cidx", "ret_count", "ret_offset", "ret_pad_off", "ret_tile_off",
     "ret_src", "crow_of_pair", "ret_rows", "x_c", "ab_c", "h_c", "dy_c", "dab", "dx_pair", "dl", "dl_sel", "wrT",
-    "sh_dab", "sh_dx", "order", "ret_order"};
+    "sh_dab", "sh_dx", "order", "ret_order", "tile_off2", "ret_tile_off2"};
 
 WsPtrs make_ptrs(const WsLayout& L, void* ws) {
   char* b = static_cast<char*>(ws);
@@ -173,6 +174,8 @@ WsPtrs make_ptrs(const WsLayout& L, void* ws) {
   p.sh_dx = nx();
   p.order = (int*)nx();
   p.ret_order = (int*)nx();
+  p.tile_off2 = (int*)nx();
+  p.ret_tile_off2 = (int*)nx();
   return p;
 }
 
@@ -419,7 +422,7 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     Span sp(st, FAM_BW);
     CKL(launch_route_topk(p.logits, router_bias, T, E, k, p.topk_idx, p.topk_w, p.masks, st));
     CKL(launch_route_scan(p.masks, (int)L.C, E, p.count, p.offset, p.pad_off, p.tile_off, p.chunk_base, p.pair_of_row,
-                         expert_offsets, st, p.order));
+                         expert_offsets, st, p.order, p.tile_off2));
     CKL(launch_route_index(p.masks, p.chunk_base, p.topk_idx, p.offset, p.pad_off, T, E, k, p.rowp_of_pair,
                           p.row_of_pair, p.pair_of_row, st));
     if (bf)
@@ -435,6 +438,7 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.rows = p.count;
     a.row_off = p.pad_off;
     a.tile_off = p.tile_off;
+    a.tile_off2 = p.tile_off2;
     a.K = H;
     a.N = F;
     a.paired = 1;
@@ -462,6 +466,7 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.rows = p.count;
     a.row_off = p.pad_off;
     a.tile_off = p.tile_off;
+    a.tile_off2 = p.tile_off2;
     a.K = F;
     a.N = H;
     a.A = p.h;
@@ -581,7 +586,7 @@ int moe_select_retained(const moe_dims* dims, void* ws, size_t ws_bytes, void* s
                                   p.score, nullptr, scores, sms, st));
     CKL(launch_select(p.score, p.count, p.pad_off, quota, E, p.ret_cidx, p.ret_count, p.status, st));
     CKL(launch_ret_scan(p.ret_count, E, p.ret_offset, p.ret_pad_off, p.ret_tile_off, p.ret_src, retained_offsets, st,
-                        p.ret_order));
+                        p.ret_order, p.ret_tile_off2));
     CKL(launch_ret_index(p.topk_idx, p.rowp_of_pair, p.row_of_pair, p.ret_cidx, p.ret_offset, p.ret_pad_off, L.P,
                         p.ret_src, p.crow_of_pair, p.ret_rows, retained_rows, sms, st));
     if (bf)
@@ -644,6 +649,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
   const int* rows = p.count;
   const int* roff = p.pad_off;
   const int* toff = p.tile_off;
+  const int* toff2 = p.tile_off2;
   const void* xs = p.x_perm;
   const void* abs_ = p.ab;
   const void* hs = p.h;
@@ -653,6 +659,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     rows = p.ret_count;
     roff = p.ret_pad_off;
     toff = p.ret_tile_off;
+    toff2 = p.ret_tile_off2;
     xs = p.x_c;
     abs_ = p.ab_c;
     hs = p.h_c;
@@ -678,6 +685,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.rows = rows;
     a.row_off = roff;
     a.tile_off = toff;
+    a.tile_off2 = toff2;
     a.K = H;
     a.N = F;
     a.A = dys;
@@ -704,6 +712,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.rows = rows;
     a.row_off = roff;
     a.tile_off = toff;
+    a.tile_off2 = toff2;
     a.K = 2 * F;
     a.N = H;
     a.A = p.dab;

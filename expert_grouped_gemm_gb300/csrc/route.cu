@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(1024) k_route_topk(float* logits, const float*
 // One block of 1024 threads, thread e = expert e.
 __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset,
                                                      int* pad_off, int* tile_off, int* chunk_base, int* pair_of_row,
-                                                     int* user_offsets, int* order) {
+                                                     int* user_offsets, int* order, int* tile_off2) {
   const int e = threadIdx.x;
   int cnt = 0;
   if (e < E)
@@ -99,10 +99,14 @@ __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int 
   if (order) block_order_desc(cnt, E, order);
   const int pad = (cnt + 15) / 16 * 16;
   const int tiles = (cnt + 127) / 128;
-  int tot_c, tot_p, tot_t;
+  const int tiles2 = (cnt + 255) / 256;
+  int tot_c, tot_p, tot_t, tot_t2;
   const int oc = block_excl_scan(e < E ? cnt : 0, &tot_c);
   const int op = block_excl_scan(e < E ? pad : 0, &tot_p);
   const int ot = block_excl_scan(e < E ? tiles : 0, &tot_t);
+  const int ot2 = block_excl_scan(e < E ? tiles2 : 0, &tot_t2);
+  if (tile_off2 && e < E) tile_off2[e] = ot2;
+  if (tile_off2 && e == 0) tile_off2[E] = tot_t2;
   if (e < E) {
     count[e] = cnt;
     offset[e] = oc;
@@ -268,9 +272,9 @@ cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, in
 
 cudaError_t launch_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset, int* pad_off,
                               int* tile_off, int* chunk_base, int* pair_of_row, int* user_offsets, cudaStream_t st,
-                              int* order) {
+                              int* order, int* tile_off2) {
   k_route_scan<<<1, 1024, 0, st>>>(masks, C, E, count, offset, pad_off, tile_off, chunk_base, pair_of_row,
-                                   user_offsets, order);
+                                   user_offsets, order, tile_off2);
   return cudaGetLastError();
 }
 
