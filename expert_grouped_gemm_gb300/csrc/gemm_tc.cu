@@ -28,18 +28,18 @@
 
 namespace moe {
 
-constexpr int kThreads = 192;
 constexpr int kStageRowBytes = 128;                   // 64 bf16 per staged row
 constexpr int kStageTileBytes = 32 * kStageRowBytes;  // one warp's 32 rows x 64 columns (4 KB)
 
-template <int BN, int STAGES, int EPI_WARP_BYTES, int CTAS>
+template <int BN, int STAGES, int EPI_WARP_BYTES, int CTAS, int NEPI>
 struct TcCfg {
+  static constexpr int THREADS = 64 + 32 * NEPI;            // producer, MMA, NEPI epilogue warps
   static constexpr int A_BYTES = kTileM * kTileK * 2;       // 16 KB: this CTA's 128 rows
   static constexpr int B_BYTES = BN * kTileK * 2 / CTAS;    // this CTA's share of the BN columns
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // per CTA
   static constexpr int TILE_M = kTileM * CTAS;              // rows of one (pair) tile
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFF = EPI_OFF + 4 * EPI_WARP_BYTES;
+  static constexpr int BAR_OFF = EPI_OFF + NEPI * EPI_WARP_BYTES;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;  // barriers + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 2 * BN;      // two accumulators
   static constexpr bool MN3D = (BN == 256);           // MN-major operands through 3-D views
@@ -125,13 +125,13 @@ __device__ __forceinline__ void aux_prefetch(uint32_t buf, const __nv_bfloat16* 
   cp_async_commit();
 }
 
-template <int BN, int STAGES, int EPI_WARP_BYTES, int EPI, int CTAS>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int STAGES, int EPI_WARP_BYTES, int EPI, int CTAS, int NEPI>
+__global__ void __launch_bounds__(64 + 32 * NEPI, 1)
     tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
                     const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO0h,
                     const __grid_constant__ CUtensorMap tmO1h, const GemmArgs args) {
-  using C = TcCfg<BN, STAGES, EPI_WARP_BYTES, CTAS>;
+  using C = TcCfg<BN, STAGES, EPI_WARP_BYTES, CTAS, NEPI>;
   constexpr bool PAIR = CTAS == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4 * CTAS);  // one arrive per epilogue warp of each CTA
+      mbar_init(&tempty[i], NEPI * CTAS);  // one arrive per epilogue warp of each CTA
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -324,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     const int row = q * 32 + lane;
-    const uint32_t wstage = smem_u32(smem + C::EPI_OFF + (warp - 2) * EPI_WARP_BYTES);
+    const int ew = warp - 2;  // epilogue warp index; with 8 warps, two share a lane quarter
+    const uint32_t wstage = smem_u32(smem + C::EPI_OFF + ew * EPI_WARP_BYTES);
     constexpr bool tma_out = EPI != EPI_F32;
     constexpr bool bwd = EPI == EPI_SWIGLU_BWD;
     constexpr bool fwd = EPI == EPI_SWIGLU_FWD;
@@ -335,6 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t aux_buf = wstage + 2 * kStageTileBytes;  // SwiGLU bwd: a and b tiles of one chunk
     const int W = args.paired ? BN / 2 : BN;                // output columns per tile
     const int CW = W / 64;                                  // 64-column chunks per tile
+    constexpr int kSplit = NEPI / 4;                        // warps sharing one lane quarter
+    const int c_begin = (ew / 4) * (CW / kSplit);           // this warp's chunks of the tile
+    const int c_end = c_begin + CW / kSplit;
     const __nv_bfloat16* ab_aux = reinterpret_cast<const __nv_bfloat16*>(args.aux);
     int acc_i = 0;
     int sc = 0;  // staging sets used so far by this warp
@@ -359,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rows_left = lim - q * 32;                    // rows of this warp's 32 that are written
       const bool real = args.var_k || m < ti.rows;           // var-M rows past the group end are zero padding
       const int64_t aux_row0 = (int64_t)ti.off + ti.m0 + q * 32;
-      if (bwd) aux_prefetch(aux_buf, ab_aux, aux_row0, args.ld_aux, args.N, ncol0, rows_left, lane);
+      if (bwd) aux_prefetch(aux_buf, ab_aux, aux_row0, args.ld_aux, args.N, ncol0 + c_begin * 64, rows_left, lane);
       const bool empty_tile = ti.kblocks == 0;  // variable-K group with no rows: output is zero
       const int acc = acc_i & 1;
       if (!empty_tile) {
@@ -369,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       const bool live = !empty_tile && real;
-      for (int c = 0; c < CW; ++c) {
+      for (int c = c_begin; c < c_end; ++c) {
         const int n0 = ncol0 + c * 64;
         const bool store = rows_left > 0 && n0 < args.N;
         uint32_t set = wstage;
@@ -457,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!tma_out) continue;
         if (bwd) {  // a|b of the next chunk lands while this one is stored
           __syncwarp();
-          if (c + 1 < CW) aux_prefetch(aux_buf, ab_aux, aux_row0, args.ld_aux, args.N, n0 + 64, rows_left, lane);
+          if (c + 1 < c_end) aux_prefetch(aux_buf, ab_aux, aux_row0, args.ld_aux, args.N, n0 + 64, rows_left, lane);
         }
         if (!store) continue;
         ++sc;
@@ -557,13 +561,15 @@ static bool make_map_mn3d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, int EPI_WARP_BYTES, int EPI, int CTAS>
+template <int BN, int STAGES, int EPI_WARP_BYTES, int EPI, int CTAS, int NEPI = 4>
 static cudaError_t launch_cfg(const GemmArgs& a, cudaStream_t st, int num_sms) {
-  using C = TcCfg<BN, STAGES, EPI_WARP_BYTES, CTAS>;
+  using C = TcCfg<BN, STAGES, EPI_WARP_BYTES, CTAS, NEPI>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
   static_assert(CTAS == 1 || BN == 256, "CTA pairs use the 256-column tile");
+  static_assert(NEPI == 4 || NEPI == 8, "four or eight epilogue warps");
   if (a.epi != EPI) return cudaErrorInvalidValue;
-  auto kern = tc_grouped_gemm<BN, STAGES, EPI_WARP_BYTES, EPI, CTAS>;
+  if (NEPI == 8 && ((a.paired ? BN / 2 : BN) / 64) % 2) return cudaErrorInvalidValue;
+  auto kern = tc_grouped_gemm<BN, STAGES, EPI_WARP_BYTES, EPI, CTAS, NEPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   CUtensorMap mA, mB0, mB1, mO0, mO1, mO0h, mO1h;
@@ -598,7 +604,7 @@ static cudaError_t launch_cfg(const GemmArgs& a, cudaStream_t st, int num_sms) {
   }
   if (!ok) return cudaErrorInvalidValue;
   if constexpr (CTAS == 1) {
-    kern<<<num_sms, kThreads, C::SMEM, st>>>(mA, mB0, mB1, mO0, mO1, mO0h, mO1h, a);
+    kern<<<num_sms, C::THREADS, C::SMEM, st>>>(mA, mB0, mB1, mO0, mO1, mO0h, mO1h, a);
     return cudaGetLastError();
   } else {
     cudaLaunchConfig_t cfg = {};
@@ -607,7 +613,7 @@ static cudaError_t launch_cfg(const GemmArgs& a, cudaStream_t st, int num_sms) {
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
     cfg.attrs = attr;
@@ -653,9 +659,9 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_s
     case EPI_STORE:
       if (need > 2 * kT) return cudaErrorInvalidValue;
       return launch_cfg<256, 4, 2 * kT, EPI_STORE, 1>(a, st, num_sms);
-    case EPI_DW:
+    case EPI_DW:  // short-K tiles: the epilogue sets the pace, so eight epilogue warps
       if (need > 2 * kT) return cudaErrorInvalidValue;
-      return launch_cfg<256, 4, 2 * kT, EPI_DW, 1>(a, st, num_sms);
+      return launch_cfg<256, 3, 2 * kT, EPI_DW, 1, 8>(a, st, num_sms);
     default:
       return cudaErrorInvalidValue;
   }
