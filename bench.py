@@ -75,6 +75,28 @@ def gemm_flops(w, R: int) -> float:
     return f
 
 
+def gemm_bytes(w, R: int) -> float:
+    """Algorithmic DRAM bytes of the grouped GEMMs of one step: every operand read
+    once, every output written once (I/O element size; fp32 router logits)."""
+    es = 2 if w.dtype == "bf16" else 4
+    T, H, F, E, P, Fs = w.T, w.H, w.F, w.E, w.P, w.F_shared
+    b = es * (T * H + H * E) + 4 * T * E                                  # router logits
+    b += es * (P * H + 2 * E * H * F + 3 * P * F)                         # gate/up -> a|b, h
+    b += es * (P * F + E * F * H + P * H)                                 # down -> y_pair
+    b += es * (R * H + E * F * H + 4 * R * F)                             # dH (reads a|b, writes da|db)
+    b += es * (2 * R * F + 2 * E * H * F + R * H)                         # dX_pair
+    if Fs:
+        b += es * (T * H + 2 * H * Fs + 3 * T * Fs) + es * (T * Fs + Fs * H + T * H)
+        b += es * (T * H + Fs * H + 4 * T * Fs) + es * (2 * T * Fs + 2 * H * Fs + T * H)
+    if not w.frozen:
+        b += es * (R * H + 2 * R * F + 2 * E * H * F)                     # dW gate/up
+        b += es * (R * F + R * H + E * F * H)                             # dW down
+        b += es * (T * H + T * E + H * E)                                 # dW router
+        if Fs:
+            b += es * (T * H + 2 * T * Fs + 2 * H * Fs) + es * (T * Fs + T * H + Fs * H)
+    return float(b)
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -336,11 +358,17 @@ def run_ours(args):
     flops = gemm_flops(w, R)
     achieved = flops / (gemm_ms_step / 1e3) / 1e12
     peak = float(peaks["bf16_tflops"])
+    gbytes = gemm_bytes(w, R)
+    hbm_ach = gbytes / (gemm_ms_step / 1e3) / 1e9
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": None, "kernel": "tc_grouped_gemm (all grouped-GEMM launches of one step)",
             "peak_source": f"{src} bf16_tflops (burst)", "gemm_ms_per_step": gemm_ms_step,
-            "bw_kernels_ms_per_step": fam_ms[1] / args.steps, "gemm_flops_per_step": flops}
-    traffic_file = os.path.join(ROOT, "profiles", "traffic.json")
+            "bw_kernels_ms_per_step": fam_ms[1] / args.steps, "gemm_flops_per_step": flops,
+            "hbm_view": {"algorithmic_bytes_per_step": gbytes, "achieved_gbs": hbm_ach,
+                         "peak_gbs": float(peaks["hbm_gbs"]), "frac": hbm_ach / float(peaks["hbm_gbs"]),
+                         "flop_per_byte": flops / gbytes,
+                         "ridge_flop_per_byte": peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)}}
+    traffic_file = os.path.join(ROOT, "profiles", "gemm_traffic.json")
     if os.path.exists(traffic_file):
         tr = json.load(open(traffic_file)).get(w.name)
         if tr and tr.get("kernel_hash") == kernel_hash():

@@ -27,10 +27,11 @@ MOE_ERR_DEVICE_ARG = -7
 MOE_BF16 = 0
 MOE_F32 = 1
 MOE_FROZEN = 1
+MOE_RECOMPUTE = 2
 
 EXPORTED = ["moe_workspace_size", "moe_fwd", "moe_select_retained", "moe_bwd", "moe_read_status",
             "moe_last_error", "moe_workspace_entry", "moe_kernel_launches", "moe_timing_enable",
-            "moe_timing_read", "moe_route_noalloc"]
+            "moe_timing_read", "moe_route_noalloc", "moe_plan_quota", "moe_selftest_wait"]
 
 
 class MoeError(RuntimeError):
@@ -69,6 +70,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                         ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]
     lib.moe_route_noalloc.argtypes = [D, vp, vp, vp, vp, i32p, f32p, i32p, i32p, i32p]
     lib.moe_route_noalloc.restype = ctypes.c_int
+    lib.moe_plan_quota.argtypes = [D, vp, ctypes.c_size_t, vp, ctypes.c_int64, ctypes.c_int64, i32p, i32p]
+    lib.moe_plan_quota.restype = ctypes.c_int
+    lib.moe_selftest_wait.argtypes = [vp, ctypes.c_int, ctypes.c_int64, i32p]
+    lib.moe_selftest_wait.restype = ctypes.c_int
     lib.moe_kernel_launches.argtypes = []
     lib.moe_kernel_launches.restype = ctypes.c_int64
     lib.moe_timing_enable.argtypes = [ctypes.c_int]
@@ -85,9 +90,9 @@ def _check(rc: int) -> None:
         raise MoeError(rc, load().moe_last_error().decode(errors="replace"))
 
 
-def make_dims(T, H, F, E, k, F_shared=0, dtype="bf16", frozen=False) -> Dims:
+def make_dims(T, H, F, E, k, F_shared=0, dtype="bf16", frozen=False, recompute=False) -> Dims:
     return Dims(T, H, F, E, k, F_shared, MOE_BF16 if dtype in ("bf16", MOE_BF16) else MOE_F32,
-                MOE_FROZEN if frozen else 0)
+                (MOE_FROZEN if frozen else 0) | (MOE_RECOMPUTE if recompute else 0))
 
 
 def _io_dtype(d: Dims):
@@ -173,6 +178,21 @@ def moe_route_noalloc(dims: Dims, x, w_router, router_bias, topk_idx, topk_w, ex
         _ptr(router_bias, "router_bias", torch.float32, False), _ptr(topk_idx, "topk_idx", torch.int32),
         _ptr(topk_w, "topk_w", torch.float32), _ptr(expert_offsets, "expert_offsets", torch.int32),
         _ptr(row_of_pair, "row_of_pair", torch.int32), _ptr(device_status, "device_status", torch.int32, False))
+    _check(rc)
+
+
+def moe_plan_quota(dims: Dims, ws: torch.Tensor, rho_num: int, rho_den: int, quota, budget=None, stream=None):
+    """Device-side retention quotas from the last forward's per-expert counts."""
+    rc = load().moe_plan_quota(ctypes.byref(dims), _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream),
+                               int(rho_num), int(rho_den), _ptr(budget, "budget", torch.int32, False),
+                               _ptr(quota, "quota", torch.int32))
+    _check(rc)
+
+
+def moe_selftest_wait(arrive: bool, limit_us: int, device_status, stream=None):
+    """One bounded barrier wait on the GPU; device_status receives MOE_OK or MOE_ERR_TIMEOUT."""
+    rc = load().moe_selftest_wait(_stream(stream), 1 if arrive else 0, int(limit_us),
+                                  _ptr(device_status, "device_status", torch.int32))
     _check(rc)
 
 

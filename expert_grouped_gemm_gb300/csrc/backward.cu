@@ -372,7 +372,26 @@ __global__ void __launch_bounds__(256) k_dx_reduce(const TIO* __restrict__ dx_pa
   }
 }
 
+// ------------------------------------------------------------------ quota planner
+// quota[e] = min(count[e], ceil(rho_num/rho_den * T*k/E)) (and <= budget[e] if given).
+__global__ void k_plan_quota(const int* count, int E, int64_t pairs, int64_t rho_num, int64_t rho_den,
+                             const int* budget, int* quota) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const int64_t den = rho_den * E;
+  const int64_t q = (rho_num * pairs + den - 1) / den;
+  int64_t v = count[e] < q ? count[e] : q;
+  if (budget) v = v < budget[e] ? v : (budget[e] > 0 ? budget[e] : 0);
+  quota[e] = (int)v;
+}
+
 // ------------------------------------------------------------------ launchers
+cudaError_t launch_plan_quota(const int* count, int E, int64_t pairs, int64_t rho_num, int64_t rho_den,
+                              const int* budget, int* quota, cudaStream_t st) {
+  k_plan_quota<<<(E + 255) / 256, 256, 0, st>>>(count, E, pairs, rho_num, rho_den, budget, quota);
+  return cudaGetLastError();
+}
+
 static int grid_for(int64_t warps, int num_sms) {
   const int64_t want = (warps + 7) / 8;
   return (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 16));

@@ -52,4 +52,7 @@ cudaError_t launch_dx_reduce(const void* dx_pair, const int* crow_of_pair, const
                              const void* wrT, const void* sh_dx, int T, int H, int k, void* dx, int num_sms,
                              cudaStream_t st);
 
+cudaError_t launch_plan_quota(const int* count, int E, int64_t pairs, int64_t rho_num, int64_t rho_den,
+                              const int* budget, int* quota, cudaStream_t st);
+
 }  // namespace moe

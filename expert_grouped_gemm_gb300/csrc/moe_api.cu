@@ -59,7 +59,7 @@ int check_dims(const moe_dims* d) {
   if (d->E > 1024) return fail(MOE_ERR_UNSUPPORTED, "E > 1024");
   if (d->F_shared < 0) return fail(MOE_ERR_INVALID_ARG, "F_shared < 0");
   if (d->dtype != MOE_BF16 && d->dtype != MOE_F32) return fail(MOE_ERR_INVALID_ARG, "unknown dtype %d", d->dtype);
-  if (d->flags & ~MOE_FROZEN) return fail(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", d->flags);
+  if (d->flags & ~(MOE_FROZEN | MOE_RECOMPUTE)) return fail(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", d->flags);
   const int64_t P = d->T * d->k;
   if (P + 16 * d->E >= (1ll << 31) - 1024) return fail(MOE_ERR_UNSUPPORTED, "T*k too large for int32 row indices");
   if (d->H >= (1 << 24) || d->F >= (1 << 24) || d->F_shared >= (1 << 24))
@@ -287,6 +287,111 @@ GemmArgs base_args(int* status) {
 
 }  // namespace
 
+// The expert forward GEMMs: gate/up with fused SwiGLU, down, and the shared
+// expert. moe_fwd runs them; in MOE_RECOMPUTE mode the retention select or the
+// backward runs them again (same kernels, same inputs: the same bits).
+int expert_forward_gemms(const WsLayout& L, const WsPtrs& p, int bf, int sms, cudaStream_t st, const void* w_gate,
+                         const void* w_up, const void* w_down, const void* ws_gate, const void* ws_up,
+                         const void* ws_down, const void* x) {
+  const int T = (int)L.T, H = (int)L.H, F = (int)L.F, E = (int)L.E, Fs = (int)L.Fs;
+  const bool shared = L.Fs > 0;
+  // expert gate/up with fused SwiGLU
+  {
+    GemmArgs a = base_args(p.status);
+    a.var_k = 0;
+    a.G = E;
+    a.rows = p.count;
+    a.row_off = p.pad_off;
+    a.tile_off = p.tile_off;
+    a.tile_off2 = p.tile_off2;
+    a.K = H;
+    a.N = F;
+    a.paired = 1;
+    a.A = p.x_perm;
+    a.lda = H;
+    a.a_rows = L.Rmax;
+    a.B0 = w_gate;
+    a.B1 = w_up;
+    a.ldb = F;
+    a.b_rows = L.E * L.H;
+    a.epi = EPI_SWIGLU_FWD;
+    a.out0 = p.ab;
+    a.ldo = 2 * F;
+    a.out1 = p.h;
+    a.ldo1 = F;
+    a.zero_pad = 1;
+    a.out_rows = L.Rmax;
+    CKL(run_gemm(a, bf, 256, st, sms));
+  }
+  // expert down
+  {
+    GemmArgs a = base_args(p.status);
+    a.var_k = 0;
+    a.G = E;
+    a.rows = p.count;
+    a.row_off = p.pad_off;
+    a.tile_off = p.tile_off;
+    a.tile_off2 = p.tile_off2;
+    a.K = F;
+    a.N = H;
+    a.A = p.h;
+    a.lda = F;
+    a.a_rows = L.Rmax;
+    a.B0 = w_down;
+    a.ldb = H;
+    a.b_rows = L.E * L.F;
+    a.epi = EPI_STORE;
+    a.out0 = p.y_pair;
+    a.ldo = H;
+    a.zero_pad = 1;
+    a.out_rows = L.Rmax;
+    CKL(run_gemm(a, bf, 256, st, sms));
+  }
+  if (shared) {
+    GemmArgs a = base_args(p.status);
+    a.var_k = 0;
+    a.G = 1;
+    a.rows_const = T;
+    a.K = H;
+    a.N = Fs;
+    a.paired = 1;
+    a.A = x;
+    a.lda = H;
+    a.a_rows = T;
+    a.B0 = ws_gate;
+    a.B1 = ws_up;
+    a.ldb = Fs;
+    a.b_rows = H;
+    a.epi = EPI_SWIGLU_FWD;
+    a.out0 = p.sh_ab;
+    a.ldo = 2 * Fs;
+    a.out1 = p.sh_h;
+    a.ldo1 = Fs;
+    a.zero_pad = 1;
+    a.out_rows = L.Tpad;
+    CKL(run_gemm(a, bf, 256, st, sms));
+    GemmArgs b = base_args(p.status);
+    b.var_k = 0;
+    b.G = 1;
+    b.rows_const = T;
+    b.K = Fs;
+    b.N = H;
+    b.A = p.sh_h;
+    b.lda = Fs;
+    b.a_rows = L.Tpad;
+    b.B0 = ws_down;
+    b.ldb = H;
+    b.b_rows = Fs;
+    b.epi = EPI_STORE;
+    b.out0 = p.sh_y;
+    b.ldo = H;
+    b.zero_pad = 1;
+    b.out_rows = L.Tpad;
+    CKL(run_gemm(b, bf, 256, st, sms));
+  }
+  return MOE_OK;
+}
+
 // Hooks for the other translation units of the library (not part of the C ABI).
 namespace moe {
 int internal_check_dims(const moe_dims* d) { return check_dims(d); }
@@ -321,6 +426,28 @@ int moe_workspace_entry(const moe_dims* dims, int i, const char** name, size_t* 
 }
 
 int64_t moe_kernel_launches(void) { return g_launches.load(); }
+
+int moe_plan_quota(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, int64_t rho_num, int64_t rho_den,
+                   const int32_t* budget, int32_t* quota) {
+  WsLayout L;
+  int rc = check_ws(dims, ws, ws_bytes, &L);
+  if (rc) return rc;
+  if ((rc = check_ptr(quota, "quota", true, 4)) || (rc = check_ptr(budget, "budget", false, 4))) return rc;
+  if (rho_num < 0 || rho_den < 1 || rho_num > (1ll << 20) || rho_den > (1ll << 20))
+    return fail(MOE_ERR_INVALID_ARG, "need 0 <= rho_num <= 2^20 and 1 <= rho_den <= 2^20");
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_state.find(ws);
+    if (it == g_state.end() || !it->second.fwd_done)
+      return fail(MOE_ERR_STATE, "moe_plan_quota before moe_fwd on this workspace");
+    if (!same_dims(it->second.d, *dims)) return fail(MOE_ERR_STATE, "dims differ from moe_fwd's");
+  }
+  const WsPtrs p = make_ptrs(L, ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Span sp(st, FAM_BW);
+  CKL(launch_plan_quota(p.count, (int)L.E, L.P, rho_num, rho_den, budget, quota, st));
+  return MOE_OK;
+}
 
 int moe_timing_enable(int on) {
   std::lock_guard<std::mutex> lk(g_timing.mu);
@@ -430,100 +557,7 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     else
       CKL(launch_gather_rows<float>(x, p.pair_of_row, p.pad_off + E, L.Rmax, H, k, p.x_perm, p.xnorm, sms, st));
   }
-  // expert gate/up with fused SwiGLU
-  {
-    GemmArgs a = base_args(p.status);
-    a.var_k = 0;
-    a.G = E;
-    a.rows = p.count;
-    a.row_off = p.pad_off;
-    a.tile_off = p.tile_off;
-    a.tile_off2 = p.tile_off2;
-    a.K = H;
-    a.N = F;
-    a.paired = 1;
-    a.A = p.x_perm;
-    a.lda = H;
-    a.a_rows = L.Rmax;
-    a.B0 = w_gate;
-    a.B1 = w_up;
-    a.ldb = F;
-    a.b_rows = L.E * L.H;
-    a.epi = EPI_SWIGLU_FWD;
-    a.out0 = p.ab;
-    a.ldo = 2 * F;
-    a.out1 = p.h;
-    a.ldo1 = F;
-    a.zero_pad = 1;
-    a.out_rows = L.Rmax;
-    CKL(run_gemm(a, bf, 256, st, sms));
-  }
-  // expert down
-  {
-    GemmArgs a = base_args(p.status);
-    a.var_k = 0;
-    a.G = E;
-    a.rows = p.count;
-    a.row_off = p.pad_off;
-    a.tile_off = p.tile_off;
-    a.tile_off2 = p.tile_off2;
-    a.K = F;
-    a.N = H;
-    a.A = p.h;
-    a.lda = F;
-    a.a_rows = L.Rmax;
-    a.B0 = w_down;
-    a.ldb = H;
-    a.b_rows = L.E * L.F;
-    a.epi = EPI_STORE;
-    a.out0 = p.y_pair;
-    a.ldo = H;
-    a.zero_pad = 1;
-    a.out_rows = L.Rmax;
-    CKL(run_gemm(a, bf, 256, st, sms));
-  }
-  if (shared) {
-    GemmArgs a = base_args(p.status);
-    a.var_k = 0;
-    a.G = 1;
-    a.rows_const = T;
-    a.K = H;
-    a.N = Fs;
-    a.paired = 1;
-    a.A = x;
-    a.lda = H;
-    a.a_rows = T;
-    a.B0 = ws_gate;
-    a.B1 = ws_up;
-    a.ldb = Fs;
-    a.b_rows = H;
-    a.epi = EPI_SWIGLU_FWD;
-    a.out0 = p.sh_ab;
-    a.ldo = 2 * Fs;
-    a.out1 = p.sh_h;
-    a.ldo1 = Fs;
-    a.zero_pad = 1;
-    a.out_rows = L.Tpad;
-    CKL(run_gemm(a, bf, 256, st, sms));
-    GemmArgs b = base_args(p.status);
-    b.var_k = 0;
-    b.G = 1;
-    b.rows_const = T;
-    b.K = Fs;
-    b.N = H;
-    b.A = p.sh_h;
-    b.lda = Fs;
-    b.a_rows = L.Tpad;
-    b.B0 = ws_down;
-    b.ldb = H;
-    b.b_rows = Fs;
-    b.epi = EPI_STORE;
-    b.out0 = p.sh_y;
-    b.ldo = H;
-    b.zero_pad = 1;
-    b.out_rows = L.Tpad;
-    CKL(run_gemm(b, bf, 256, st, sms));
-  }
+  if ((rc = expert_forward_gemms(L, p, bf, sms, st, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, x))) return rc;
   {
     Span sp(st, FAM_BW);
     if (bf)
@@ -576,6 +610,9 @@ int moe_select_retained(const moe_dims* dims, void* ws, size_t ws_bytes, void* s
   const int bf = dims->dtype == MOE_BF16;
   const int sms = num_sms_current();
   const int H = (int)L.H, F = (int)L.F, E = (int)L.E, k = (int)L.k;
+  if (dims->flags & MOE_RECOMPUTE)  // scores and compaction read y_pair, a|b and h: re-derive them
+    if ((rc = expert_forward_gemms(L, p, bf, sms, st, s.w_gate, s.w_up, s.w_down, s.ws_gate, s.ws_up, s.ws_down, s.x)))
+      return rc;
   {
     Span sp(st, FAM_BW);
     if (bf)
@@ -665,6 +702,12 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     hs = p.h_c;
     dys = p.dy_c;
     crow = p.crow_of_pair;
+  }
+  if ((dims->flags & MOE_RECOMPUTE) && !use_retained) {
+    // the backward re-derives a|b, h and y_pair from the saved permuted rows (with
+    // use_retained the selection already did, before it compacted them)
+    if ((rc = expert_forward_gemms(L, p, bf, sms, st, s.w_gate, s.w_up, s.w_down, s.ws_gate, s.ws_up, s.ws_down, x)))
+      return rc;
   }
   if (!use_retained) {
     // router-gradient dots g (and scores) over all pairs plus the w*dY rows;

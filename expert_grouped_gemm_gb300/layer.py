@@ -15,11 +15,15 @@ WEIGHTS = ["w_router", "w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down"
 
 
 class MoELayer:
-    def __init__(self, w: Workload, params: dict, device="cuda", record_routing: bool = False):
-        """params: CPU or device tensors named as in inputs.make_inputs (weights + optional router_bias)."""
+    def __init__(self, w: Workload, params: dict, device="cuda", record_routing: bool = False,
+                 recompute: bool = False):
+        """params: CPU or device tensors named as in inputs.make_inputs (weights + optional router_bias).
+
+        recompute: the backward re-derives the expert activations instead of
+        using the forward's (the keep-nothing mode, MOE_RECOMPUTE)."""
         self.w = w
         self.device = torch.device(device)
-        self.dims = _lib.make_dims(w.T, w.H, w.F, w.E, w.k, w.F_shared, w.dtype, w.frozen)
+        self.dims = _lib.make_dims(w.T, w.H, w.F, w.E, w.k, w.F_shared, w.dtype, w.frozen, recompute)
         self.io = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         dev = self.device
         self.p = {}

@@ -65,6 +65,9 @@ typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
 /* dims.flags */
 #define MOE_FROZEN 1u   /* experts and router frozen ([I14] Scope: LoRA first): no dW of any
                            expert, router or shared expert is computed; dX stays complete */
+#define MOE_RECOMPUTE 2u /* [PR44] keep_graph=False: the backward (or the retention select)
+                           re-derives a|b, h and y_pair from the saved permuted rows instead
+                           of using the forward's; results are bitwise the same */
 
 typedef struct moe_dims {
   int64_t T;         /* tokens */
@@ -196,6 +199,28 @@ MOE_API int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* strea
 MOE_API int moe_route_noalloc(const moe_dims* dims, void* stream, const void* x, const void* w_router,
                               const float* router_bias, int32_t* topk_idx, float* topk_w,
                               int32_t* expert_offsets, int32_t* row_of_pair, int32_t* device_status);
+
+/*
+ * moe_plan_quota -- per-expert retention quotas planned on the device from the
+ * routing of the last moe_fwd ([LRMoE] Abstract: the forward plans retention
+ * quotas under resource constraints).
+ *   quota[e] = min(count_e, ceil(rho_num / rho_den * T*k / E)), and at most
+ *   budget[e] when budget (int32 [E] device, nullable) is given (negative
+ *   budgets count as 0). quota[E] int32 device output, usable directly by
+ *   moe_select_retained. 0 <= rho_num <= 2^20, 1 <= rho_den <= 2^20.
+ */
+MOE_API int moe_plan_quota(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, int64_t rho_num,
+                           int64_t rho_den, const int32_t* budget, int32_t* quota);
+
+/*
+ * moe_selftest_wait -- checks, on the GPU, the bounded barrier wait that every
+ * pipelined kernel of the library uses. A one-thread kernel waits on an
+ * mbarrier; with arrive != 0 it arrives first and *device_status becomes
+ * MOE_OK, with arrive == 0 nothing arrives, the wait gives up after limit_us
+ * (1 .. 1,000,000) and *device_status becomes MOE_ERR_TIMEOUT. The kernel
+ * always returns, so the context stays usable. device_status: one int32 on the device.
+ */
+MOE_API int moe_selftest_wait(void* stream, int arrive, int64_t limit_us, int32_t* device_status);
 
 /*
  * moe_read_status -- synchronises `stream` and returns the device status word
