@@ -31,6 +31,11 @@ namespace moe {
 constexpr int kStageRowBytes = 128;                   // 64 bf16 per staged row
 constexpr int kStageTileBytes = 32 * kStageRowBytes;  // one warp's 32 rows x 64 columns (4 KB)
 
+// CTAs per 256-column tile for the expert GEMMs (1: one CTA; 2: CTA pair, M = 256).
+#ifndef MOE_GEMM_CTAS
+#define MOE_GEMM_CTAS 1
+#endif
+
 template <int BN, int STAGES, int EPI_WARP_BYTES, int CTAS, int NEPI>
 struct TcCfg {
   static constexpr int THREADS = 64 + 32 * NEPI;            // producer, MMA, NEPI epilogue warps
@@ -649,6 +654,24 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_s
     return cudaErrorInvalidValue;
   }
   // 256-column tiles (the CTA-pair variant, CTAS = 2, is kept but measured slower)
+#if MOE_GEMM_CTAS == 2
+  switch (a.epi) {
+    case EPI_SWIGLU_BWD:
+      if (need > 4 * kT) return cudaErrorInvalidValue;
+      return launch_cfg<256, 5, 4 * kT, EPI_SWIGLU_BWD, 2>(a, st, num_sms);
+    case EPI_SWIGLU_FWD:
+      if (need > 2 * kT) return cudaErrorInvalidValue;
+      return launch_cfg<256, 6, 2 * kT, EPI_SWIGLU_FWD, 2>(a, st, num_sms);
+    case EPI_STORE:
+      if (need > 2 * kT) return cudaErrorInvalidValue;
+      return launch_cfg<256, 6, 2 * kT, EPI_STORE, 2>(a, st, num_sms);
+    case EPI_DW:
+      if (need > 2 * kT) return cudaErrorInvalidValue;
+      return launch_cfg<256, 6, 2 * kT, EPI_DW, 2>(a, st, num_sms);
+    default:
+      return cudaErrorInvalidValue;
+  }
+#else
   switch (a.epi) {
     case EPI_SWIGLU_BWD:
       if (need > 4 * kT) return cudaErrorInvalidValue;
@@ -665,6 +688,7 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_s
     default:
       return cudaErrorInvalidValue;
   }
+#endif
 }
 
 }  // namespace moe
