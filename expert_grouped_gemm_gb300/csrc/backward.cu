@@ -303,31 +303,30 @@ __global__ void k_transpose(const TIO* in, int R, int Cc, TIO* out) {
 }
 
 // ------------------------------------------------------------------ dX reduce
-// Warp per token: dX_t = sum_j [kept] dx_pair[crow(t,j)] + sum_j dl_j W_r[:,e_j] (+ shared dX_t).
-// Rows of up to 8 slots are loaded together before they are summed (slot order kept).
+// dX_t = sum_j [kept] dx_pair[crow(t,j)] + sum_j dl_j W_r[:,e_j] (+ shared dX_t),
+// slots in order. bf16: block per token, thread per 8-column slice, the rows of
+// up to 8 slots loaded together before they are summed.
 template <typename TIO>
 __global__ void __launch_bounds__(256) k_dx_reduce(const TIO* __restrict__ dx_pair, const int* __restrict__ crow_of_pair,
                                                    const int* __restrict__ topk_idx, const float* __restrict__ dl_sel,
                                                    const TIO* __restrict__ wrT, const TIO* __restrict__ sh_dx, int T,
                                                    int H, int k, TIO* __restrict__ dx) {
-  const int lane = threadIdx.x & 31;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
-    const int64_t p0 = (int64_t)t * k;
-    TIO* dst = dx + (int64_t)t * H;
-    if constexpr (sizeof(TIO) == 2) {
-      for (int i = lane; i < H / 8; i += 32) {
+  if constexpr (sizeof(TIO) == 2) {
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+      const int64_t p0 = (int64_t)t * k;
+      for (int i = threadIdx.x; i < H / 8; i += blockDim.x) {
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, f[8];
         for (int j0 = 0; j0 < k; j0 += 8) {
           uint4 u[8];
+          int cr[8];
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            u[jj] = make_uint4(0, 0, 0, 0);
-            const int cr = (j0 + jj < k) ? crow_of_pair[p0 + j0 + jj] : -1;
-            if (cr >= 0) u[jj] = reinterpret_cast<const uint4*>(dx_pair + (int64_t)cr * H)[i];
+            cr[jj] = (j0 + jj < k) ? crow_of_pair[p0 + j0 + jj] : -1;
+            u[jj] = cr[jj] >= 0 ? reinterpret_cast<const uint4*>(dx_pair + (int64_t)cr[jj] * H)[i] : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            if (j0 + jj < k && crow_of_pair[p0 + j0 + jj] >= 0) {
+            if (cr[jj] >= 0) {
               bf16x8_to_f(u[jj], f);
 #pragma unroll
               for (int q = 0; q < 8; ++q) acc[q] += f[q];
@@ -354,9 +353,13 @@ __global__ void __launch_bounds__(256) k_dx_reduce(const TIO* __restrict__ dx_pa
 #pragma unroll
           for (int q = 0; q < 8; ++q) acc[q] += f[q];
         }
-        reinterpret_cast<uint4*>(dst)[i] = f_to_bf16x8(acc);
+        reinterpret_cast<uint4*>(dx + (int64_t)t * H)[i] = f_to_bf16x8(acc);
       }
-    } else {
+    }
+  } else {
+    const int lane = threadIdx.x & 31;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
+      const int64_t p0 = (int64_t)t * k;
       for (int i = lane; i < H; i += 32) {
         float acc = 0.0f;
         for (int j = 0; j < k; ++j) {
@@ -366,7 +369,7 @@ __global__ void __launch_bounds__(256) k_dx_reduce(const TIO* __restrict__ dx_pa
         for (int j = 0; j < k; ++j)
           acc = fmaf(dl_sel[p0 + j], io<TIO>::to_f(wrT[(int64_t)topk_idx[p0 + j] * H + i]), acc);
         if (sh_dx) acc += io<TIO>::to_f(sh_dx[(int64_t)t * H + i]);
-        dst[i] = io<TIO>::cvt(acc);
+        dx[(int64_t)t * H + i] = io<TIO>::cvt(acc);
       }
     }
   }
@@ -462,7 +465,9 @@ template <typename TIO>
 cudaError_t launch_dx_reduce(const void* dx_pair, const int* crow_of_pair, const int* topk_idx, const float* dl_sel,
                              const void* wrT, const void* sh_dx, int T, int H, int k, void* dx, int num_sms,
                              cudaStream_t st) {
-  k_dx_reduce<TIO><<<grid_for(T, num_sms), 256, 0, st>>>(
+  const int grid = sizeof(TIO) == 2 ? (int)std::max<int64_t>(1, std::min<int64_t>(T, (int64_t)num_sms * 32))
+                                    : grid_for(T, num_sms);
+  k_dx_reduce<TIO><<<grid, 256, 0, st>>>(
       reinterpret_cast<const TIO*>(dx_pair), crow_of_pair, topk_idx, dl_sel, reinterpret_cast<const TIO*>(wrT),
       reinterpret_cast<const TIO*>(sh_dx), T, H, k, reinterpret_cast<TIO*>(dx));
   return cudaGetLastError();

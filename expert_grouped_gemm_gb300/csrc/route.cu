@@ -19,83 +19,91 @@ namespace moe {
 constexpr int kChunk = 64;  // tokens per routing chunk (one bit each in a uint64 mask)
 
 // ------------------------------------------------------------------ top-k
-// grid = C chunks of 64 tokens, block = 1024 (32 warps, two tokens each).
-// Warp per token; lane l holds logits e = l + 32 i (i < EPL) in registers.
+// Warp per token (8 per block); lane l holds logits e = l + 32 i (i < EPL) in
+// registers. The chunk masks (zeroed by the launcher) get one bit per pair.
 template <int EPL>
-__global__ void __launch_bounds__(1024) k_route_topk(float* logits, const float* bias, int T, int E, int k,
-                                                     int* topk_idx, float* topk_w, uint64_t* masks) {
-  extern __shared__ uint64_t smask[];  // [E]
-  const int c = blockIdx.x;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) smask[e] = 0ull;
-  __syncthreads();
+__global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* bias, int T, int E, int k,
+                                                    int* topk_idx, float* topk_w, uint64_t* masks) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int tl = warp; tl < kChunk; tl += 32) {
-    const int t = c * kChunk + tl;
-    if (t >= T) break;
-    float* lrow = logits + (int64_t)t * E;
-    float v[EPL];
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  float* lrow = logits + (int64_t)t * E;
+  float v[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float x = lrow[e] + (bias ? bias[e] : 0.0f);
+      lrow[e] = x;                     // the biased logits the selection used
+      v[i] = (x != x) ? -INFINITY : x;  // NaN ranks last
+    }
+  }
+  uint32_t taken = 0;  // bit i: expert lane + 32 i already selected (or absent)
+#pragma unroll
+  for (int i = 0; i < EPL; ++i)
+    if (lane + 32 * i >= E) taken |= 1u << i;
+  float lmax = 0.0f, sum = 0.0f;
+  uint64_t* cmask = masks + (int64_t)(t / kChunk) * E;
+  const uint64_t bit = 1ull << (t % kChunk);
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
-      if (e < E) {
-        const float x = lrow[e] + (bias ? bias[e] : 0.0f);
-        lrow[e] = x;                     // the biased logits the selection used
-        v[i] = (x != x) ? -INFINITY : x;  // NaN ranks last
+      if (!((taken >> i) & 1u) && (be == 0x7fffffff || v[i] > bv)) {  // e ascending: ties keep the first
+        bv = v[i];
+        be = e;
       }
     }
-    uint32_t taken = 0;  // bit i: expert lane + 32 i already selected (or absent)
 #pragma unroll
-    for (int i = 0; i < EPL; ++i)
-      if (lane + 32 * i >= E) taken |= 1u << i;
-    float lmax = 0.0f, sum = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        if (!((taken >> i) & 1u) && (be == 0x7fffffff || v[i] > bv)) {  // e ascending: ties keep the first
-          bv = v[i];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == 0) {
-        if (j == 0) lmax = bv;
-        const float ex = expf(bv - lmax);
-        sum += ex;
-        topk_idx[(int64_t)t * k + j] = be;
-        topk_w[(int64_t)t * k + j] = ex;
-        atomicOr(reinterpret_cast<unsigned long long*>(&smask[be]), 1ull << tl);
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
+        bv = ov;
+        be = oe;
       }
     }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
     if (lane == 0) {
-      const float inv = 1.0f / sum;
-      for (int j = 0; j < k; ++j) topk_w[(int64_t)t * k + j] *= inv;
+      if (j == 0) lmax = bv;
+      const float ex = expf(bv - lmax);
+      sum += ex;
+      topk_idx[(int64_t)t * k + j] = be;
+      topk_w[(int64_t)t * k + j] = ex;
+      atomicOr(reinterpret_cast<unsigned long long*>(&cmask[be]), bit);
     }
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) masks[(int64_t)c * E + e] = smask[e];
+  if (lane == 0) {
+    const float inv = 1.0f / sum;
+    for (int j = 0; j < k; ++j) topk_w[(int64_t)t * k + j] *= inv;
+  }
 }
 
 // ------------------------------------------------------------------ scan
-// One block of 1024 threads, thread e = expert e.
+// One block of 1024 threads: expert e is handled by `parts` threads, each owning
+// a contiguous range of chunks (parts = 1024 / E rounded down to a power of two).
 __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset,
                                                      int* pad_off, int* tile_off, int* chunk_base, int* pair_of_row,
                                                      int* user_offsets, int* order, int* tile_off2) {
-  const int e = threadIdx.x;
+  __shared__ int part_cnt[1024];
+  int parts = 1;
+  while (parts * 2 * E <= 1024) parts *= 2;
+  const int tid = threadIdx.x;
+  const int pe = tid % E, pp = tid / E;
+  const bool worker = tid < parts * E;
+  const int per = (C + parts - 1) / parts;
+  const int c0 = pp * per, c1 = min(C, c0 + per);
+  int pc = 0;
+  if (worker)
+    for (int c = c0; c < c1; ++c) pc += __popcll(masks[(int64_t)c * E + pe]);
+  if (worker) part_cnt[pp * E + pe] = pc;
+  __syncthreads();
+  const int e = tid;
   int cnt = 0;
   if (e < E)
-    for (int c = 0; c < C; ++c) cnt += __popcll(masks[(int64_t)c * E + e]);
+    for (int p = 0; p < parts; ++p) cnt += part_cnt[p * E + e];
   if (order) block_order_desc(cnt, E, order);
   const int pad = (cnt + 15) / 16 * 16;
   const int tiles = (cnt + 127) / 128;
@@ -105,26 +113,32 @@ __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int 
   const int op = block_excl_scan(e < E ? pad : 0, &tot_p);
   const int ot = block_excl_scan(e < E ? tiles : 0, &tot_t);
   const int ot2 = block_excl_scan(e < E ? tiles2 : 0, &tot_t2);
-  if (tile_off2 && e < E) tile_off2[e] = ot2;
-  if (tile_off2 && e == 0) tile_off2[E] = tot_t2;
+  __shared__ int s_pad[1024];
   if (e < E) {
     count[e] = cnt;
     offset[e] = oc;
     pad_off[e] = op;
     tile_off[e] = ot;
+    if (tile_off2) tile_off2[e] = ot2;
     if (user_offsets) user_offsets[e] = oc;
-    int run = op;
-    for (int c = 0; c < C; ++c) {
-      chunk_base[(int64_t)c * E + e] = run;
-      run += __popcll(masks[(int64_t)c * E + e]);
-    }
+    s_pad[e] = op;
     for (int r = op + cnt; r < op + pad; ++r) pair_of_row[r] = -1;
   }
   if (e == 0) {
     offset[E] = tot_c;
     pad_off[E] = tot_p;
     tile_off[E] = tot_t;
+    if (tile_off2) tile_off2[E] = tot_t2;
     if (user_offsets) user_offsets[E] = tot_c;
+  }
+  __syncthreads();
+  if (worker) {
+    int run = s_pad[pe];
+    for (int p = 0; p < pp; ++p) run += part_cnt[p * E + pe];
+    for (int c = c0; c < c1; ++c) {
+      chunk_base[(int64_t)c * E + pe] = run;
+      run += __popcll(masks[(int64_t)c * E + pe]);
+    }
   }
 }
 
@@ -202,19 +216,18 @@ __global__ void __launch_bounds__(256) k_gather_rows(const TIO* x, const int* pa
 }
 
 // ------------------------------------------------------------------ combine
-// Warp per token: y[t] = sum_j w[t,j] y_pair[row(t,j)] (+ shared y[t]), slots ascending.
-// The rows of up to 8 slots are loaded together before they are summed.
+// y[t] = sum_j w[t,j] y_pair[row(t,j)] (+ shared y[t]), slots ascending.
+// bf16: block per token, thread per 8-column slice; the k rows of a slice are
+// loaded together (up to 8 at a time) before they are summed.
 template <typename TIO>
 __global__ void __launch_bounds__(256) k_combine(const TIO* __restrict__ y_pair, const int* __restrict__ rowp_of_pair,
                                                  const float* __restrict__ topk_w, const TIO* __restrict__ sh_y, int T,
                                                  int H, int k, TIO* __restrict__ y) {
-  const int lane = threadIdx.x & 31;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
-    TIO* dst = y + (int64_t)t * H;
-    const int64_t p0 = (int64_t)t * k;
-    if constexpr (sizeof(TIO) == 2) {
-      const int nv = H / 8;
-      for (int i = lane; i < nv; i += 32) {
+  if constexpr (sizeof(TIO) == 2) {
+    const int nv = H / 8;
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+      const int64_t p0 = (int64_t)t * k;
+      for (int i = threadIdx.x; i < nv; i += blockDim.x) {
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         for (int j0 = 0; j0 < k; j0 += 8) {
           uint4 u[8];
@@ -238,18 +251,19 @@ __global__ void __launch_bounds__(256) k_combine(const TIO* __restrict__ y_pair,
 #pragma unroll
           for (int q = 0; q < 8; ++q) acc[q] += f[q];
         }
-        reinterpret_cast<uint4*>(dst)[i] = f_to_bf16x8(acc);
+        reinterpret_cast<uint4*>(y + (int64_t)t * H)[i] = f_to_bf16x8(acc);
       }
-    } else {
+    }
+  } else {
+    const int lane = threadIdx.x & 31;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
+      const int64_t p0 = (int64_t)t * k;
       for (int i = lane; i < H; i += 32) {
         float acc = 0.0f;
-        for (int j = 0; j < k; ++j) {
-          const float w = topk_w[p0 + j];
-          const int r = rowp_of_pair[p0 + j];
-          acc = fmaf(w, io<TIO>::to_f(y_pair[(int64_t)r * H + i]), acc);
-        }
+        for (int j = 0; j < k; ++j)
+          acc = fmaf(topk_w[p0 + j], io<TIO>::to_f(y_pair[(int64_t)rowp_of_pair[p0 + j] * H + i]), acc);
         if (sh_y) acc += io<TIO>::to_f(sh_y[(int64_t)t * H + i]);
-        dst[i] = io<TIO>::cvt(acc);
+        y[(int64_t)t * H + i] = io<TIO>::cvt(acc);
       }
     }
   }
@@ -259,14 +273,16 @@ __global__ void __launch_bounds__(256) k_combine(const TIO* __restrict__ y_pair,
 cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, int k, int* topk_idx, float* topk_w,
                               uint64_t* masks, cudaStream_t st) {
   const int C = (T + kChunk - 1) / kChunk;
-  const size_t sm = E * sizeof(uint64_t);
+  cudaError_t e = cudaMemsetAsync(masks, 0, (size_t)C * E * sizeof(uint64_t), st);
+  if (e != cudaSuccess) return e;
+  const int grid = (T + 7) / 8;
   const int epl = (E + 31) / 32;
-  if (epl <= 1) k_route_topk<1><<<C, 1024, sm, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
-  else if (epl <= 2) k_route_topk<2><<<C, 1024, sm, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
-  else if (epl <= 4) k_route_topk<4><<<C, 1024, sm, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
-  else if (epl <= 8) k_route_topk<8><<<C, 1024, sm, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
-  else if (epl <= 16) k_route_topk<16><<<C, 1024, sm, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
-  else k_route_topk<32><<<C, 1024, sm, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  if (epl <= 1) k_route_topk<1><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  else if (epl <= 2) k_route_topk<2><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  else if (epl <= 4) k_route_topk<4><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  else if (epl <= 8) k_route_topk<8><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  else if (epl <= 16) k_route_topk<16><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  else k_route_topk<32><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
   return cudaGetLastError();
 }
 
@@ -301,8 +317,13 @@ cudaError_t launch_gather_rows(const void* x, const int* pair_of_row, const int*
 template <typename TIO>
 cudaError_t launch_combine(const void* y_pair, const int* rowp_of_pair, const float* topk_w, const void* sh_y, int T,
                            int H, int k, void* y, int num_sms, cudaStream_t st) {
-  const int64_t want = ((int64_t)T + 7) / 8;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 16));
+  int grid;
+  if (sizeof(TIO) == 2) {
+    grid = (int)std::max<int64_t>(1, std::min<int64_t>(T, (int64_t)num_sms * 32));
+  } else {
+    const int64_t want = ((int64_t)T + 7) / 8;
+    grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 16));
+  }
   k_combine<TIO><<<grid, 256, 0, st>>>(reinterpret_cast<const TIO*>(y_pair), rowp_of_pair, topk_w,
                                        reinterpret_cast<const TIO*>(sh_y), T, H, k, reinterpret_cast<TIO*>(y));
   return cudaGetLastError();
