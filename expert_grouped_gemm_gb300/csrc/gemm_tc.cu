@@ -338,7 +338,8 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
     const int nout = (fwd || bwd || (EPI == EPI_DW && args.paired)) ? 2 : 1;
     // one output alternates two staging sets when room allows; otherwise one set
     const int nbuf = (nout == 1 && EPI_WARP_BYTES >= 2 * kStageTileBytes) ? 2 : 1;
-    const uint32_t aux_buf = wstage + 2 * kStageTileBytes;  // SwiGLU bwd: a and b tiles of one chunk
+    // SwiGLU bwd: the a and b tiles of one chunk; da and db are staged in place over them
+    const uint32_t aux_buf = wstage;
     const int W = args.paired ? BN / 2 : BN;                // output columns per tile
     const int CW = W / 64;                                  // 64-column chunks per tile
     constexpr int kSplit = NEPI / 4;                        // warps sharing one lane quarter
@@ -368,7 +369,11 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
       const int rows_left = lim - q * 32;                    // rows of this warp's 32 that are written
       const bool real = args.var_k || m < ti.rows;           // var-M rows past the group end are zero padding
       const int64_t aux_row0 = (int64_t)ti.off + ti.m0 + q * 32;
-      if (bwd) aux_prefetch(aux_buf, ab_aux, aux_row0, args.ld_aux, args.N, ncol0 + c_begin * 64, rows_left, lane);
+      if (bwd) {  // the previous tile's last da|db stores must have read the aux tiles
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        aux_prefetch(aux_buf, ab_aux, aux_row0, args.ld_aux, args.N, ncol0 + c_begin * 64, rows_left, lane);
+      }
       const bool empty_tile = ti.kblocks == 0;  // variable-K group with no rows: output is zero
       const int acc = acc_i & 1;
       if (!empty_tile) {
@@ -382,7 +387,7 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
         const int n0 = ncol0 + c * 64;
         const bool store = rows_left > 0 && n0 < args.N;
         uint32_t set = wstage;
-        if (tma_out && store) {
+        if (tma_out && store && !bwd) {
           set = wstage + (nbuf == 2 ? (uint32_t)((sc & 1) * kStageTileBytes) : 0u);
           // the set must be free: the bulk stores that last used it have read it
           if (lane == 0) {
@@ -452,9 +457,9 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
                 da[i] = x0[i] * bv[i] * s * (1.0f + av[i] * (1.0f - s));
                 db[i] = x0[i] * av[i] * s;
               }
-              if (store) {
-                st_shared_v4(set + stage_off(lane, j), f_to_bf16x8(da));
-                st_shared_v4(set + kStageTileBytes + stage_off(lane, j), f_to_bf16x8(db));
+              if (store) {  // in place: each thread overwrites only what it just read
+                st_shared_v4(aux_buf + stage_off(lane, j), f_to_bf16x8(da));
+                st_shared_v4(aux_buf + kStageTileBytes + stage_off(lane, j), f_to_bf16x8(db));
               }
             } else {  // EPI_DW / EPI_STORE
               if (!store) continue;
@@ -464,11 +469,13 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
           }
         }
         if (!tma_out) continue;
-        if (bwd) {  // a|b of the next chunk lands while this one is stored
-          __syncwarp();
-          if (c + 1 < c_end) aux_prefetch(aux_buf, ab_aux, aux_row0, args.ld_aux, args.N, n0 + 64, rows_left, lane);
+        if (!store) {
+          if (bwd && c + 1 < c_end) {
+            __syncwarp();
+            aux_prefetch(aux_buf, ab_aux, aux_row0, args.ld_aux, args.N, n0 + 64, rows_left, lane);
+          }
+          continue;
         }
-        if (!store) continue;
         ++sc;
         fence_async_smem();
         __syncwarp();
@@ -482,6 +489,11 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
           tma_store_2d(o0, set, n0, (int)out_row0);
           if (nout > 1) tma_store_2d(o1, set + kStageTileBytes, c1, (int)out_row0);
           bulk_commit();
+        }
+        if (bwd && c + 1 < c_end) {  // the a|b tiles are free once da|db have been read out
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          aux_prefetch(aux_buf, ab_aux, aux_row0, args.ld_aux, args.N, n0 + 64, rows_left, lane);
         }
         if (fwd) {  // h goes out through the a tile once a|b have been read from it
           if (lane == 0) bulk_wait_read_all();
@@ -640,7 +652,7 @@ static cudaError_t launch_cfg(const GemmArgs& a, cudaStream_t st, int num_sms) {
 static int staging_bytes(const GemmArgs& a) {
   if (a.epi == EPI_F32) return 0;
   if (a.epi == EPI_SWIGLU_FWD) return 2 * kStageTileBytes;
-  if (a.epi == EPI_SWIGLU_BWD) return 2 * kStageTileBytes + 2 * kStageTileBytes;
+  if (a.epi == EPI_SWIGLU_BWD) return 2 * kStageTileBytes;  // a|b tiles, da|db staged in place
   return ((a.epi == EPI_DW && a.paired) ? 2 : 1) * kStageTileBytes;
 }
 
@@ -674,8 +686,8 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_s
 #else
   switch (a.epi) {
     case EPI_SWIGLU_BWD:
-      if (need > 4 * kT) return cudaErrorInvalidValue;
-      return launch_cfg<256, 3, 4 * kT, EPI_SWIGLU_BWD, 1>(a, st, num_sms);
+      if (need > 2 * kT) return cudaErrorInvalidValue;
+      return launch_cfg<256, 4, 2 * kT, EPI_SWIGLU_BWD, 1>(a, st, num_sms);
     case EPI_SWIGLU_FWD:
       if (need > 2 * kT) return cudaErrorInvalidValue;
       return launch_cfg<256, 4, 2 * kT, EPI_SWIGLU_FWD, 1>(a, st, num_sms);
