@@ -47,7 +47,11 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+// Logistic function with the hardware exponential and the approximate divide
+// (a few ulp in fp32, far inside the bf16 storage precision; the limits 0 and
+// 1 come out exactly for large |z|). The IEEE divide costs several times more
+// and made the SwiGLU epilogues slower than the MMAs they overlap.
+__device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 // Record the first device-side error into the workspace status word.
 __device__ __forceinline__ void set_status(int* status, int code) {
