@@ -148,10 +148,10 @@ __global__ void __launch_bounds__(256) k_select(const float* score, const int* c
 // One block of 1024 threads: offsets of the kept rows, exact and padded.
 __global__ void __launch_bounds__(1024) k_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off,
                                                    int* ret_tile_off, int* ret_src, int* user_offsets, int* order,
-                                                   int* ret_tile_off2) {
+                                                   int* ret_tile_off2, int4* tile_rec, int4* ord_rec) {
   const int e = threadIdx.x;
   const int cnt = e < E ? ret_count[e] : 0;
-  if (order) block_order_desc(cnt, E, order);
+  const int rank = order ? block_order_desc(cnt, E, order) : 0;
   const int pad = (cnt + 15) / 16 * 16;
   const int tiles = (cnt + 127) / 128;
   const int tiles2 = (cnt + 255) / 256;
@@ -168,6 +168,9 @@ __global__ void __launch_bounds__(1024) k_ret_scan(const int* ret_count, int E, 
     ret_tile_off[e] = ot;
     if (user_offsets) user_offsets[e] = oc;
     for (int r = op + cnt; r < op + pad; ++r) ret_src[r] = -1;
+    if (tile_rec)
+      for (int j = 0; j < tiles; ++j) tile_rec[ot + j] = make_int4(e, j * 128, cnt, op);
+    if (ord_rec && order) ord_rec[rank] = make_int4(e, cnt, op, 0);
   }
   if (e == 0) {
     ret_offset[E] = tc;
@@ -417,9 +420,10 @@ cudaError_t launch_select(const float* score, const int* count, const int* pad_o
 }
 
 cudaError_t launch_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off, int* ret_tile_off,
-                            int* ret_src, int* user_offsets, cudaStream_t st, int* order, int* ret_tile_off2) {
+                            int* ret_src, int* user_offsets, cudaStream_t st, int* order, int* ret_tile_off2,
+                            int4* tile_rec, int4* ord_rec) {
   k_ret_scan<<<1, 1024, 0, st>>>(ret_count, E, ret_offset, ret_pad_off, ret_tile_off, ret_src, user_offsets, order,
-                                 ret_tile_off2);
+                                 ret_tile_off2, tile_rec, ord_rec);
   return cudaGetLastError();
 }
 

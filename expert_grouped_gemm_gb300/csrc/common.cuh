@@ -89,13 +89,13 @@ __device__ __forceinline__ int block_excl_scan(int v, int* total) {
 
 // Block-wide (blockDim.x >= E, <= 1024): order[rank] = e with ranks by value
 // descending, ties to the lower index. Deterministic; O(E) per thread.
-__device__ __forceinline__ void block_order_desc(int v, int E, int* order) {
+__device__ __forceinline__ int block_order_desc(int v, int E, int* order) {
   __shared__ int s_val[1024];
   const int e = threadIdx.x;
   if (e < E) s_val[e] = v;
   __syncthreads();
+  int rank = 0;
   if (e < E) {
-    int rank = 0;
     for (int j = 0; j < E; ++j) {
       const int u = s_val[j];
       rank += (u > v) || (u == v && j < e);
@@ -103,6 +103,7 @@ __device__ __forceinline__ void block_order_desc(int v, int E, int* order) {
     order[rank] = e;
   }
   __syncthreads();
+  return rank;
 }
 
 // ---------------------------------------------------------------- PTX wrappers

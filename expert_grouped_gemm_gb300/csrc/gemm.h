@@ -60,6 +60,11 @@ struct GemmArgs {
   int zero_pad;         // var-M: write zeros in rows [rows_g, round16(rows_g))
   int64_t out_rows;     // rows of the out0 / out1 2-D views (tensor-core stores are clipped there)
   const int* g_order;   // var-K: order in which groups are scheduled (heaviest first), or null
+  // Tile records (read with one 16-byte load instead of a search): var-M, one per
+  // 128-row block {group, first row within the group, rows, row offset}; var-K,
+  // one per scheduled group {group, rows, row offset, 0}. Null: derive from the above.
+  const int4* tile_rec;
+  const int4* grp_rec;
   int* status;
 };
 

@@ -60,20 +60,46 @@ __device__ __forceinline__ int n_tiles(const GemmArgs& a) {
   return (a.N + w - 1) / w;
 }
 
+// The record behind tile t (one 16-byte load), when the schedule has records;
+// the roles load the next tile's record while they work on the current one, so
+// the load latency stays off their critical path.
 template <int BN, int TILE_M>
-__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int NT) {
+__device__ __forceinline__ int4 load_tile_rec(const GemmArgs& a, int t, int NT) {
+  if (a.var_k) {
+    if (a.grp_rec) return __ldg(a.grp_rec + t / (((a.M + TILE_M - 1) / TILE_M) * NT));
+  } else if (TILE_M == kTileM && a.tile_rec) {
+    return __ldg(a.tile_rec + t / NT);
+  }
+  return make_int4(0, 0, 0, 0);
+}
+
+template <int BN, int TILE_M>
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int NT, int4 rec) {
   TileInfo ti;
   const int* toff = TILE_M == kTileM ? a.tile_off : a.tile_off2;
   if (a.var_k) {
     const int MT = (a.M + TILE_M - 1) / TILE_M;
     const int gi = t / (MT * NT);
     const int rem = t - gi * MT * NT;
-    ti.g = a.g_order ? a.g_order[gi] : gi;
     ti.m0 = (rem / NT) * TILE_M;
     ti.nt = rem % NT;
-    ti.rows = grp_rows(a, ti.g);
-    ti.off = grp_off(a, ti.g);
+    if (a.grp_rec) {
+      ti.g = rec.x;
+      ti.rows = rec.y;
+      ti.off = rec.z;
+    } else {
+      ti.g = a.g_order ? a.g_order[gi] : gi;
+      ti.rows = grp_rows(a, ti.g);
+      ti.off = grp_off(a, ti.g);
+    }
     ti.kblocks = (ti.rows + kTileK - 1) / kTileK;
+  } else if (TILE_M == kTileM && a.tile_rec) {
+    ti.nt = t - (t / NT) * NT;
+    ti.g = rec.x;
+    ti.m0 = rec.y;
+    ti.rows = rec.z;
+    ti.off = rec.w;
+    ti.kblocks = a.K / kTileK;
   } else {
     const int u = t / NT;
     ti.nt = t - u * NT;
@@ -206,8 +232,10 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
       if constexpr (PAIR) tma_load_3d_pair(dst, map, bar, c0, c1, c2);
       else tma_load_3d(dst, map, bar, c0, c1, c2);
     };
+    int4 rec = cluster_id < total ? load_tile_rec<BN, C::TILE_M>(args, cluster_id, NT) : make_int4(0, 0, 0, 0);
     for (int t = cluster_id; t < total && ok; t += num_clusters) {
-      const TileInfo ti = decode_tile<BN, C::TILE_M>(args, t, NT);
+      const TileInfo ti = decode_tile<BN, C::TILE_M>(args, t, NT, rec);
+      if (t + num_clusters < total) rec = load_tile_rec<BN, C::TILE_M>(args, t + num_clusters, NT);
       const int m0c = ti.m0 + (int)rank * kTileM;  // this CTA's rows (var-M) / columns (var-K) of A
       for (int kb = 0; kb < ti.kblocks; ++kb) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -278,12 +306,26 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
   } else if (warp == 1 && lane == 0 && leader) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16(C::TILE_M, BN, args.var_k, args.b_kmajor ? 0 : 1);
+    // shared-memory descriptors of stage 0; a K-major operand advances 32 bytes per
+    // k16 step, an MN-major one (a 3-D box of 64-row chunks) 2048 bytes
+    const uint32_t sa0 = smem_u32(smem);
+    const uint64_t adesc0 = args.var_k ? sdesc_sw128(sa0, 8192, 1024) : sdesc_sw128(sa0, 16, 1024);
+    const uint64_t bdesc0 =
+        args.b_kmajor ? sdesc_sw128(sa0 + C::A_BYTES, 16, 1024) : sdesc_sw128(sa0 + C::A_BYTES, 8192, 1024);
+    const uint64_t astep = args.var_k ? 2048 >> 4 : 32 >> 4;
+    const uint64_t bstep = args.b_kmajor ? 32 >> 4 : 2048 >> 4;
+    auto mma = [&](uint32_t d, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+      if constexpr (PAIR) tc_mma_bf16_pair(d, a_desc, b_desc, idesc, accumulate);
+      else tc_mma_bf16(d, a_desc, b_desc, idesc, accumulate);
+    };
     int stage = 0;
     uint32_t phase = 0;
     int acc_i = 0;
     bool ok = true;
+    int4 rec = cluster_id < total ? load_tile_rec<BN, C::TILE_M>(args, cluster_id, NT) : make_int4(0, 0, 0, 0);
     for (int t = cluster_id; t < total && ok; t += num_clusters) {
-      const TileInfo ti = decode_tile<BN, C::TILE_M>(args, t, NT);
+      const TileInfo ti = decode_tile<BN, C::TILE_M>(args, t, NT, rec);
+      if (t + num_clusters < total) rec = load_tile_rec<BN, C::TILE_M>(args, t + num_clusters, NT);
       if (ti.kblocks == 0) continue;
       const int acc = acc_i & 1;
       const uint32_t acc_par = (uint32_t)((acc_i >> 1) & 1);
@@ -298,16 +340,18 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
-        const uint32_t sb = sa + C::A_BYTES;
-        int nk = kTileK / 16;
-        if (args.var_k && kb == ti.kblocks - 1) nk = (ti.rows - kb * kTileK + 15) / 16;
-        for (int kk = 0; kk < nk; ++kk) {
-          const uint64_t ad = args.var_k ? sdesc_sw128(sa + kk * 2048, 8192, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
-          const uint64_t bd =
-              args.b_kmajor ? sdesc_sw128(sb + kk * 32, 16, 1024) : sdesc_sw128(sb + kk * 2048, 8192, 1024);
-          if constexpr (PAIR) tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-          else tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+        // descriptors of this stage: the k16 steps only move the start address
+        const uint64_t ad = adesc0 + (uint64_t)(stage * (C::STAGE_BYTES >> 4));
+        const uint64_t bd = bdesc0 + (uint64_t)(stage * (C::STAGE_BYTES >> 4));
+        const uint32_t acc0 = kb != 0 ? 1u : 0u;
+        if (!(args.var_k && kb == ti.kblocks - 1)) {  // full k-block: four k16 steps
+          mma(d_tmem, ad, bd, acc0);
+          mma(d_tmem, ad + astep, bd + bstep, 1u);
+          mma(d_tmem, ad + 2 * astep, bd + 2 * bstep, 1u);
+          mma(d_tmem, ad + 3 * astep, bd + 3 * bstep, 1u);
+        } else {  // a variable-K group's last k-block: its rows rounded up to 16
+          const int nk = (ti.rows - kb * kTileK + 15) / 16;
+          for (int kk = 0; kk < nk; ++kk) mma(d_tmem, ad + kk * astep, bd + kk * bstep, kk != 0 ? 1u : acc0);
         }
         if constexpr (PAIR) tc_commit_pair_mc(&empty[stage]);
         else tc_commit(&empty[stage]);
@@ -351,8 +395,10 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
     uint32_t ra[32], rb[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) rb[i] = 0u;  // only paired modes load it
+    int4 rec = cluster_id < total ? load_tile_rec<BN, C::TILE_M>(args, cluster_id, NT) : make_int4(0, 0, 0, 0);
     for (int t = cluster_id; t < total; t += num_clusters) {
-      TileInfo ti = decode_tile<BN, C::TILE_M>(args, t, NT);
+      TileInfo ti = decode_tile<BN, C::TILE_M>(args, t, NT, rec);
+      if (t + num_clusters < total) rec = load_tile_rec<BN, C::TILE_M>(args, t + num_clusters, NT);
       ti.m0 += (int)rank * kTileM;  // this CTA's 128 rows of the (pair) tile
       const int m = ti.m0 + row;
       const int ncol0 = ti.nt * W;

@@ -12,7 +12,8 @@ cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, in
                               uint64_t* masks, cudaStream_t st);
 cudaError_t launch_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset, int* pad_off,
                               int* tile_off, int* chunk_base, int* pair_of_row, int* user_offsets, cudaStream_t st,
-                              int* order = nullptr, int* tile_off2 = nullptr);
+                              int* order = nullptr, int* tile_off2 = nullptr, int4* tile_rec = nullptr,
+                              int4* ord_rec = nullptr);
 cudaError_t launch_route_index(const uint64_t* masks, const int* chunk_base, const int* topk_idx, const int* offset,
                                const int* pad_off, int T, int E, int k, int* rowp_of_pair, int* row_of_pair,
                                int* pair_of_row, cudaStream_t st);
@@ -31,7 +32,7 @@ cudaError_t launch_select(const float* score, const int* count, const int* pad_o
                           int* ret_cidx, int* ret_count, int* status, cudaStream_t st);
 cudaError_t launch_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off, int* ret_tile_off,
                             int* ret_src, int* user_offsets, cudaStream_t st, int* order = nullptr,
-                            int* ret_tile_off2 = nullptr);
+                            int* ret_tile_off2 = nullptr, int4* tile_rec = nullptr, int4* ord_rec = nullptr);
 cudaError_t launch_ret_index(const int* topk_idx, const int* rowp_of_pair, const int* row_of_pair,
                              const int* ret_cidx, const int* ret_offset, const int* ret_pad_off, int64_t P,
                              int* ret_src, int* crow_of_pair, int* ret_rows, int* user_rows, int num_sms,

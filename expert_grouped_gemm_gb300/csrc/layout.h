@@ -59,6 +59,10 @@ struct WsPtrs {
   int* ret_order;       // [E] experts by kept count, descending
   int* tile_off2;       // [E+1] prefix of ceil(count/256) (two-CTA tiles)
   int* ret_tile_off2;   // [E+1] prefix of ceil(kept/256)
+  int4* tile_rec;       // [P/128 + E] per 128-row block: {expert, first row in the group, count, pad_off}
+  int4* ret_tile_rec;   // same for the kept rows
+  int4* ord_rec;        // [E] experts in dW order: {expert, count, pad_off, 0}
+  int4* ret_ord_rec;    // same for the kept rows
 };
 
 struct WsLayout {

@@ -105,6 +105,8 @@ WsLayout make_layout(const moe_dims* d) {
       Tp * 2 * Fs * es, Tp * H * es,       // sh_dab sh_dx
       E * 4, E * 4,                        // order ret_order
       (E + 1) * 4, (E + 1) * 4,            // tile_off2 ret_tile_off2
+      (P / 128 + E + 1) * 16, (P / 128 + E + 1) * 16,  // tile_rec ret_tile_rec
+      E * 16, E * 16,                                  // ord_rec ret_ord_rec
   };
   L.n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   size_t off = 0;
@@ -122,7 +124,8 @@ const char* const kEntryNames[] = {
     "tile_off", "rowp_of_pair", "row_of_pair", "pair_of_row", "x_perm", "ab", "h", "y_pair", "sh_ab", "sh_h",
     "sh_y", "g", "score", "dy_perm", "ret_cidx", "ret_count", "ret_offset", "ret_pad_off", "ret_tile_off",
     "ret_src", "crow_of_pair", "ret_rows", "x_c", "ab_c", "h_c", "dy_c", "dab", "dx_pair", "dl", "dl_sel", "wrT",
-    "sh_dab", "sh_dx", "order", "ret_order", "tile_off2", "ret_tile_off2"};
+    "sh_dab", "sh_dx", "order", "ret_order", "tile_off2", "ret_tile_off2", "tile_rec", "ret_tile_rec", "ord_rec",
+    "ret_ord_rec"};
 
 WsPtrs make_ptrs(const WsLayout& L, void* ws) {
   char* b = static_cast<char*>(ws);
@@ -176,6 +179,10 @@ WsPtrs make_ptrs(const WsLayout& L, void* ws) {
   p.ret_order = (int*)nx();
   p.tile_off2 = (int*)nx();
   p.ret_tile_off2 = (int*)nx();
+  p.tile_rec = (int4*)nx();
+  p.ret_tile_rec = (int4*)nx();
+  p.ord_rec = (int4*)nx();
+  p.ret_ord_rec = (int4*)nx();
   return p;
 }
 
@@ -303,6 +310,7 @@ int expert_forward_gemms(const WsLayout& L, const WsPtrs& p, int bf, int sms, cu
     a.rows = p.count;
     a.row_off = p.pad_off;
     a.tile_off = p.tile_off;
+    a.tile_rec = p.tile_rec;
     a.tile_off2 = p.tile_off2;
     a.K = H;
     a.N = F;
@@ -331,6 +339,7 @@ int expert_forward_gemms(const WsLayout& L, const WsPtrs& p, int bf, int sms, cu
     a.rows = p.count;
     a.row_off = p.pad_off;
     a.tile_off = p.tile_off;
+    a.tile_rec = p.tile_rec;
     a.tile_off2 = p.tile_off2;
     a.K = F;
     a.N = H;
@@ -549,7 +558,7 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     Span sp(st, FAM_BW);
     CKL(launch_route_topk(p.logits, router_bias, T, E, k, p.topk_idx, p.topk_w, p.masks, st));
     CKL(launch_route_scan(p.masks, (int)L.C, E, p.count, p.offset, p.pad_off, p.tile_off, p.chunk_base, p.pair_of_row,
-                         expert_offsets, st, p.order, p.tile_off2));
+                         expert_offsets, st, p.order, p.tile_off2, p.tile_rec, p.ord_rec));
     CKL(launch_route_index(p.masks, p.chunk_base, p.topk_idx, p.offset, p.pad_off, T, E, k, p.rowp_of_pair,
                           p.row_of_pair, p.pair_of_row, st));
     if (bf)
@@ -623,7 +632,7 @@ int moe_select_retained(const moe_dims* dims, void* ws, size_t ws_bytes, void* s
                                   p.score, nullptr, scores, sms, st));
     CKL(launch_select(p.score, p.count, p.pad_off, quota, E, p.ret_cidx, p.ret_count, p.status, st));
     CKL(launch_ret_scan(p.ret_count, E, p.ret_offset, p.ret_pad_off, p.ret_tile_off, p.ret_src, retained_offsets, st,
-                        p.ret_order, p.ret_tile_off2));
+                        p.ret_order, p.ret_tile_off2, p.ret_tile_rec, p.ret_ord_rec));
     CKL(launch_ret_index(p.topk_idx, p.rowp_of_pair, p.row_of_pair, p.ret_cidx, p.ret_offset, p.ret_pad_off, L.P,
                         p.ret_src, p.crow_of_pair, p.ret_rows, retained_rows, sms, st));
     if (bf)
@@ -687,6 +696,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
   const int* roff = p.pad_off;
   const int* toff = p.tile_off;
   const int* toff2 = p.tile_off2;
+  const int4* trec = p.tile_rec;
   const void* xs = p.x_perm;
   const void* abs_ = p.ab;
   const void* hs = p.h;
@@ -696,6 +706,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     rows = p.ret_count;
     roff = p.ret_pad_off;
     toff = p.ret_tile_off;
+    trec = p.ret_tile_rec;
     toff2 = p.ret_tile_off2;
     xs = p.x_c;
     abs_ = p.ab_c;
@@ -728,6 +739,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.rows = rows;
     a.row_off = roff;
     a.tile_off = toff;
+    a.tile_rec = trec;
     a.tile_off2 = toff2;
     a.K = H;
     a.N = F;
@@ -755,6 +767,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.rows = rows;
     a.row_off = roff;
     a.tile_off = toff;
+    a.tile_rec = trec;
     a.tile_off2 = toff2;
     a.K = 2 * F;
     a.N = H;
@@ -859,6 +872,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
       a.ldo = F;
       a.out_gstride = L.H * L.F;
       a.g_order = use_retained ? p.ret_order : p.order;
+      a.grp_rec = use_retained ? p.ret_ord_rec : p.ord_rec;
       CKL(run_gemm(a, bf, 256, st, sms));
     }
     // dW_down[e] = h_e^T dy_e
@@ -881,6 +895,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
       a.ldo = H;
       a.out_gstride = L.F * L.H;
       a.g_order = use_retained ? p.ret_order : p.order;
+      a.grp_rec = use_retained ? p.ret_ord_rec : p.ord_rec;
       CKL(run_gemm(a, bf, 256, st, sms));
     }
     // dW_router = x^T dl

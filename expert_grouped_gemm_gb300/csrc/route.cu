@@ -86,7 +86,8 @@ __global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* 
 // a contiguous range of chunks (parts = 1024 / E rounded down to a power of two).
 __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset,
                                                      int* pad_off, int* tile_off, int* chunk_base, int* pair_of_row,
-                                                     int* user_offsets, int* order, int* tile_off2) {
+                                                     int* user_offsets, int* order, int* tile_off2,
+                                                     int4* tile_rec, int4* ord_rec) {
   __shared__ int part_cnt[1024];
   int parts = 1;
   while (parts * 2 * E <= 1024) parts *= 2;
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int 
   int cnt = 0;
   if (e < E)
     for (int p = 0; p < parts; ++p) cnt += part_cnt[p * E + e];
-  if (order) block_order_desc(cnt, E, order);
+  const int rank = order ? block_order_desc(cnt, E, order) : 0;
   const int pad = (cnt + 15) / 16 * 16;
   const int tiles = (cnt + 127) / 128;
   const int tiles2 = (cnt + 255) / 256;
@@ -123,6 +124,9 @@ __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int 
     if (user_offsets) user_offsets[e] = oc;
     s_pad[e] = op;
     for (int r = op + cnt; r < op + pad; ++r) pair_of_row[r] = -1;
+    if (tile_rec)
+      for (int j = 0; j < tiles; ++j) tile_rec[ot + j] = make_int4(e, j * 128, cnt, op);
+    if (ord_rec && order) ord_rec[rank] = make_int4(e, cnt, op, 0);
   }
   if (e == 0) {
     offset[E] = tot_c;
@@ -288,9 +292,9 @@ cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, in
 
 cudaError_t launch_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset, int* pad_off,
                               int* tile_off, int* chunk_base, int* pair_of_row, int* user_offsets, cudaStream_t st,
-                              int* order, int* tile_off2) {
+                              int* order, int* tile_off2, int4* tile_rec, int4* ord_rec) {
   k_route_scan<<<1, 1024, 0, st>>>(masks, C, E, count, offset, pad_off, tile_off, chunk_base, pair_of_row,
-                                   user_offsets, order, tile_off2);
+                                   user_offsets, order, tile_off2, tile_rec, ord_rec);
   return cudaGetLastError();
 }
 
