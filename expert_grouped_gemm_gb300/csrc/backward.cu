@@ -465,10 +465,95 @@ cudaError_t launch_transpose(const void* in, int R, int Cc, void* out, cudaStrea
   return cudaGetLastError();
 }
 
+// bf16, k <= 8: persistent blocks; the next token's slot metadata is loaded by k
+// threads while this token's rows are in flight and handed over through shared
+// memory at the token boundary. Same summation order as k_dx_reduce.
+__global__ void __launch_bounds__(256, 3) k_dx_reduce_k8(const __nv_bfloat16* __restrict__ dx_pair,
+                                                      const int* __restrict__ crow_of_pair,
+                                                      const int* __restrict__ topk_idx, const float* __restrict__ dl_sel,
+                                                      const __nv_bfloat16* __restrict__ wrT,
+                                                      const __nv_bfloat16* __restrict__ sh_dx, int T, int H, int k,
+                                                      __nv_bfloat16* __restrict__ dx) {
+  __shared__ int s_c[2][8], s_e[2][8];
+  __shared__ float s_d[2][8];
+  const int tid = threadIdx.x;
+  int t = blockIdx.x, buf = 0;
+  if (tid < 8) {
+    const bool v = tid < k && t < T;
+    s_c[0][tid] = v ? crow_of_pair[(int64_t)t * k + tid] : -1;
+    s_e[0][tid] = v ? topk_idx[(int64_t)t * k + tid] : 0;
+    s_d[0][tid] = v ? dl_sel[(int64_t)t * k + tid] : 0.0f;
+  }
+  __syncthreads();
+  for (; t < T; t += gridDim.x) {
+    const int tn = t + gridDim.x;
+    int c_next = -1, e_next = 0;
+    float d_next = 0.0f;
+    if (tid < k && tn < T) {
+      c_next = crow_of_pair[(int64_t)tn * k + tid];
+      e_next = topk_idx[(int64_t)tn * k + tid];
+      d_next = dl_sel[(int64_t)tn * k + tid];
+    }
+    for (int i = tid; i < H / 8; i += blockDim.x) {
+      uint4 u[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int cr = s_c[buf][j];
+        u[j] = cr >= 0 ? reinterpret_cast<const uint4*>(dx_pair + (int64_t)cr * H)[i] : make_uint4(0, 0, 0, 0);
+      }
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, f[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (s_c[buf][j] >= 0) {
+          bf16x8_to_f(u[j], f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] += f[q];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < k) u[j] = reinterpret_cast<const uint4*>(wrT + (int64_t)s_e[buf][j] * H)[i];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j < k) {
+          bf16x8_to_f(u[j], f);
+          const float d = s_d[buf][j];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = fmaf(d, f[q], acc[q]);
+        }
+      }
+      if (sh_dx) {
+        bf16x8_to_f(reinterpret_cast<const uint4*>(sh_dx + (int64_t)t * H)[i], f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] += f[q];
+      }
+      reinterpret_cast<uint4*>(dx + (int64_t)t * H)[i] = f_to_bf16x8(acc);
+    }
+    if (tid < 8) {
+      s_c[buf ^ 1][tid] = c_next;
+      s_e[buf ^ 1][tid] = e_next;
+      s_d[buf ^ 1][tid] = d_next;
+    }
+    __syncthreads();
+    buf ^= 1;
+  }
+}
+
 template <typename TIO>
 cudaError_t launch_dx_reduce(const void* dx_pair, const int* crow_of_pair, const int* topk_idx, const float* dl_sel,
                              const void* wrT, const void* sh_dx, int T, int H, int k, void* dx, int num_sms,
                              cudaStream_t st) {
+  if (sizeof(TIO) == 2 && k <= 8) {
+    int per_sm = 0;  // persistent: as many blocks as fit at once
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_dx_reduce_k8, 256, 0) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    const int g = (int)std::max<int64_t>(1, std::min<int64_t>(T, (int64_t)num_sms * per_sm));
+    k_dx_reduce_k8<<<g, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(dx_pair), crow_of_pair, topk_idx, dl_sel,
+                                      reinterpret_cast<const __nv_bfloat16*>(wrT),
+                                      reinterpret_cast<const __nv_bfloat16*>(sh_dx), T, H, k,
+                                      reinterpret_cast<__nv_bfloat16*>(dx));
+    return cudaGetLastError();
+  }
   const int grid = sizeof(TIO) == 2 ? (int)std::max<int64_t>(1, std::min<int64_t>(T, (int64_t)num_sms * 32))
                                     : grid_for(T, num_sms);
   k_dx_reduce<TIO><<<grid, 256, 0, st>>>(

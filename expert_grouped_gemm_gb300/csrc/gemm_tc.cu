@@ -224,74 +224,77 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
     bool ok = true;
-    auto load2 = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
-      if constexpr (PAIR) tma_load_2d_pair(dst, map, bar, c0, c1);
-      else tma_load_2d(dst, map, bar, c0, c1);
-    };
-    auto load3 = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1, int c2) {
-      if constexpr (PAIR) tma_load_3d_pair(dst, map, bar, c0, c1, c2);
-      else tma_load_3d(dst, map, bar, c0, c1, c2);
+    // Every TMA box of k-block kb of tile ti, loaded into the stage at sa with
+    // completion on the barrier fb.
+    auto issue = [&](const TileInfo& ti, int kb, uint32_t sa, uint32_t fb) {
+      auto load2 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1) {
+        if constexpr (PAIR) tma_load_2d_pair(dst, map, fb, c0, c1);
+        else tma_load_2d(dst, map, fb, c0, c1);
+      };
+      auto load3 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2) {
+        if constexpr (PAIR) tma_load_3d_pair(dst, map, fb, c0, c1, c2);
+        else tma_load_3d(dst, map, fb, c0, c1, c2);
+      };
+      const int m0c = ti.m0 + (int)rank * kTileM;  // this CTA's rows (var-M) / columns (var-K) of A
+      const uint32_t sb = sa + C::A_BYTES;
+      // A
+      if (!args.var_k) {
+        load2(sa, &tmA, kb * kTileK, ti.off + m0c);
+      } else if (C::MN3D) {
+        load3(sa, &tmA, 0, ti.off + kb * kTileK, m0c / 64);
+      } else {
+        load2(sa, &tmA, m0c, ti.off + kb * kTileK);
+        load2(sa + 8192, &tmA, m0c + 64, ti.off + kb * kTileK);
+      }
+      // B (a pair splits the BN columns: rank 0 the first half, rank 1 the second)
+      if (args.b_kmajor) {
+        const bool second = args.k_split > 0 && kb * kTileK >= args.k_split;
+        const int kk = second ? kb - args.k_split / kTileK : kb;
+        load2(sb, second ? &tmB1 : &tmB0, kk * kTileK, ti.g * args.N + ti.nt * BN + (int)rank * (BN / CTAS));
+      } else {
+        const int brow = args.var_k ? ti.off + kb * kTileK : ti.g * args.K + kb * kTileK;
+        if (C::MN3D) {
+          if (args.paired) {  // halves of BN/2 columns: B0, then B1 at column offset b1_col
+            if (!PAIR || rank == 0) load3(sb, &tmB0, 0, brow, ti.nt * (BN / 128));
+            if (!PAIR || rank == 1)
+              load3(PAIR ? sb : sb + BN / 2 * 128, &tmB1, 0, brow, args.b1_col / 64 + ti.nt * (BN / 128));
+          } else {
+            load3(sb, &tmB0, 0, brow, ti.nt * (BN / 64) + (int)rank * (BN / 64 / CTAS));
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c) {
+            int col;
+            const CUtensorMap* map = &tmB0;
+            if (args.paired) {
+              const int half = c / (BN / 128);
+              col = ti.nt * (BN / 2) + (c % (BN / 128)) * 64;
+              if (half) {
+                map = &tmB1;
+                col += args.b1_col;
+              }
+            } else {
+              col = ti.nt * BN + c * 64;
+            }
+            load2(sb + c * 8192, map, col, brow);
+          }
+        }
+      }
     };
     int4 rec = cluster_id < total ? load_tile_rec<BN, C::TILE_M>(args, cluster_id, NT) : make_int4(0, 0, 0, 0);
     for (int t = cluster_id; t < total && ok; t += num_clusters) {
       const TileInfo ti = decode_tile<BN, C::TILE_M>(args, t, NT, rec);
       if (t + num_clusters < total) rec = load_tile_rec<BN, C::TILE_M>(args, t + num_clusters, NT);
-      const int m0c = ti.m0 + (int)rank * kTileM;  // this CTA's rows (var-M) / columns (var-K) of A
       for (int kb = 0; kb < ti.kblocks; ++kb) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
-        uint8_t* sa = smem + stage * C::STAGE_BYTES;
-        uint8_t* sb = sa + C::A_BYTES;
+        const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
         const uint32_t fb = full0 + stage * 8;  // the leader's full barrier of this stage
         if (leader) mbar_arrive_expect_tx(&full[stage], CTAS * C::STAGE_BYTES);
         issued_parity[stage] = (int)phase;
-        // A
-        if (!args.var_k) {
-          load2(smem_u32(sa), &tmA, fb, kb * kTileK, ti.off + m0c);
-        } else if (C::MN3D) {
-          load3(smem_u32(sa), &tmA, fb, 0, ti.off + kb * kTileK, m0c / 64);
-        } else {
-          load2(smem_u32(sa), &tmA, fb, m0c, ti.off + kb * kTileK);
-          load2(smem_u32(sa + 8192), &tmA, fb, m0c + 64, ti.off + kb * kTileK);
-        }
-        // B (a pair splits the BN columns: rank 0 the first half, rank 1 the second)
-        if (args.b_kmajor) {
-          const bool second = args.k_split > 0 && kb * kTileK >= args.k_split;
-          const int kk = second ? kb - args.k_split / kTileK : kb;
-          load2(smem_u32(sb), second ? &tmB1 : &tmB0, fb, kk * kTileK,
-                ti.g * args.N + ti.nt * BN + (int)rank * (BN / CTAS));
-        } else {
-          const int brow = args.var_k ? ti.off + kb * kTileK : ti.g * args.K + kb * kTileK;
-          if (C::MN3D) {
-            if (args.paired) {  // halves of BN/2 columns: B0, then B1 at column offset b1_col
-              if (!PAIR || rank == 0) load3(smem_u32(sb), &tmB0, fb, 0, brow, ti.nt * (BN / 128));
-              if (!PAIR || rank == 1)
-                load3(smem_u32(PAIR ? sb : sb + BN / 2 * 128), &tmB1, fb, 0, brow,
-                      args.b1_col / 64 + ti.nt * (BN / 128));
-            } else {
-              load3(smem_u32(sb), &tmB0, fb, 0, brow, ti.nt * (BN / 64) + (int)rank * (BN / 64 / CTAS));
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c) {
-              int col;
-              const CUtensorMap* map = &tmB0;
-              if (args.paired) {
-                const int half = c / (BN / 128);
-                col = ti.nt * (BN / 2) + (c % (BN / 128)) * 64;
-                if (half) {
-                  map = &tmB1;
-                  col += args.b1_col;
-                }
-              } else {
-                col = ti.nt * BN + c * 64;
-              }
-              load2(smem_u32(sb + c * 8192), map, fb, col, brow);
-            }
-          }
-        }
+        issue(ti, kb, sa, fb);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;

@@ -273,6 +273,65 @@ __global__ void __launch_bounds__(256) k_combine(const TIO* __restrict__ y_pair,
   }
 }
 
+// bf16, k <= 8: persistent blocks, thread per 8-column slice. The next token's
+// row indices and weights are loaded (by k threads, into registers) while this
+// token's rows are in flight and handed over through shared memory at the token
+// boundary, so no block stalls on an index load before its row loads. Same
+// summation order as k_combine.
+__global__ void __launch_bounds__(256, 4) k_combine_k8(const __nv_bfloat16* __restrict__ y_pair,
+                                                    const int* __restrict__ rowp_of_pair, const float* __restrict__ topk_w,
+                                                    const __nv_bfloat16* __restrict__ sh_y, int T, int H, int k,
+                                                    __nv_bfloat16* __restrict__ y) {
+  __shared__ int s_row[2][8];
+  __shared__ float s_w[2][8];
+  const int tid = threadIdx.x, nv = H / 8;
+  int t = blockIdx.x, buf = 0;
+  if (tid < k && t < T) {
+    s_row[0][tid] = rowp_of_pair[(int64_t)t * k + tid];
+    s_w[0][tid] = topk_w[(int64_t)t * k + tid];
+  }
+  __syncthreads();
+  for (; t < T; t += gridDim.x) {
+    const int tn = t + gridDim.x;
+    int r_next = 0;
+    float w_next = 0.0f;
+    if (tid < k && tn < T) {
+      r_next = rowp_of_pair[(int64_t)tn * k + tid];
+      w_next = topk_w[(int64_t)tn * k + tid];
+    }
+    for (int i = tid; i < nv; i += blockDim.x) {
+      uint4 u[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < k) u[j] = reinterpret_cast<const uint4*>(y_pair + (int64_t)s_row[buf][j] * H)[i];
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j < k) {
+          float f[8];
+          bf16x8_to_f(u[j], f);
+          const float w = s_w[buf][j];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = fmaf(w, f[q], acc[q]);
+        }
+      }
+      if (sh_y) {
+        float f[8];
+        bf16x8_to_f(reinterpret_cast<const uint4*>(sh_y + (int64_t)t * H)[i], f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] += f[q];
+      }
+      reinterpret_cast<uint4*>(y + (int64_t)t * H)[i] = f_to_bf16x8(acc);
+    }
+    if (tid < k) {
+      s_row[buf ^ 1][tid] = r_next;
+      s_w[buf ^ 1][tid] = w_next;
+    }
+    __syncthreads();
+    buf ^= 1;
+  }
+}
+
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, int k, int* topk_idx, float* topk_w,
                               uint64_t* masks, cudaStream_t st) {
@@ -321,6 +380,16 @@ cudaError_t launch_gather_rows(const void* x, const int* pair_of_row, const int*
 template <typename TIO>
 cudaError_t launch_combine(const void* y_pair, const int* rowp_of_pair, const float* topk_w, const void* sh_y, int T,
                            int H, int k, void* y, int num_sms, cudaStream_t st) {
+  if (sizeof(TIO) == 2 && k <= 8) {
+    int per_sm = 0;  // persistent: as many blocks as fit at once
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_combine_k8, 256, 0) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    const int g = (int)std::max<int64_t>(1, std::min<int64_t>(T, (int64_t)num_sms * per_sm));
+    k_combine_k8<<<g, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(y_pair), rowp_of_pair, topk_w,
+                                    reinterpret_cast<const __nv_bfloat16*>(sh_y), T, H, k,
+                                    reinterpret_cast<__nv_bfloat16*>(y));
+    return cudaGetLastError();
+  }
   int grid;
   if (sizeof(TIO) == 2) {
     grid = (int)std::max<int64_t>(1, std::min<int64_t>(T, (int64_t)num_sms * 32));
