@@ -77,7 +77,7 @@ typedef struct moe_dims {
   int64_t k;         /* experts per token, 1 <= k <= E <= 1024 */
   int64_t F_shared;  /* always-on shared expert intermediate size; 0 = none */
   int32_t dtype;     /* moe_dtype */
-  uint32_t flags;    /* MOE_FROZEN */
+  uint32_t flags;    /* MOE_FROZEN | MOE_RECOMPUTE */
 } moe_dims;
 
 /*
