@@ -19,12 +19,16 @@ enum Epi : int {
   EPI_STORE = 1,       // var-M: out0 [rows, ldo] in the I/O type
   EPI_SWIGLU_BWD = 2,  // var-M: acc = dh; aux = ab [rows, 2N]; out0 = dAB [rows, 2N] (da | db)
   EPI_DW = 3,          // var-K: out0 (+ out1 when paired) [G][M][ldo] in the I/O type
-  EPI_F32 = 4,         // var-M: out0 fp32 [rows, ldo]
+  EPI_F32 = 4,         // fp32 out0 [rows, ldo] (var-M rows of the group; var-K rows g*M + m); with a K
+                       // split, split s writes out0 + s * part_stride and a reduce pass adds the splits
+                       // in order; paired: the second half at column N
 };
 
 constexpr int kPadRows = 16;  // per-group row padding of permuted buffers
 constexpr int kTileM = 128;   // tensor-core tile rows
 constexpr int kTileK = 64;    // tensor-core k-block (one 128-byte swizzle row of bf16)
+constexpr int kMaxSplit = 16; // largest K split of a tensor-core GEMM
+constexpr int kSplitMaxSms = 256;  // the workspace holds K-split partials for GPUs of up to this many SMs
 
 struct GemmArgs {
   // schedule
@@ -65,6 +69,10 @@ struct GemmArgs {
   // one per scheduled group {group, rows, row offset, 0}. Null: derive from the above.
   const int4* tile_rec;
   const int4* grp_rec;
+  // K split (tensor cores, EPI_F32 only): every tile's k-blocks are divided over ksplit
+  // CTAs (0 or 1: none); a split without k-blocks writes zeros
+  int ksplit;
+  int64_t part_stride;  // elements between the fp32 outputs of consecutive splits
   int* status;
 };
 

@@ -50,8 +50,10 @@ struct TcCfg {
   static constexpr bool MN3D = (BN == 256);           // MN-major operands through 3-D views
 };
 
+// kb0 / kblocks: this tile's k-blocks (all of them without a K split); kb_last:
+// the group's last k-block (variable K: the one a group's rows end in)
 struct TileInfo {
-  int g, m0, nt, rows, off, kblocks;
+  int g, m0, nt, rows, off, kblocks, kb0, kb_last, split;
 };
 
 template <int BN>
@@ -65,6 +67,7 @@ __device__ __forceinline__ int n_tiles(const GemmArgs& a) {
 // the load latency stays off their critical path.
 template <int BN, int TILE_M>
 __device__ __forceinline__ int4 load_tile_rec(const GemmArgs& a, int t, int NT) {
+  if (a.ksplit > 1) t /= a.ksplit;
   if (a.var_k) {
     if (a.grp_rec) return __ldg(a.grp_rec + t / (((a.M + TILE_M - 1) / TILE_M) * NT));
   } else if (TILE_M == kTileM && a.tile_rec) {
@@ -77,6 +80,9 @@ template <int BN, int TILE_M>
 __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int NT, int4 rec) {
   TileInfo ti;
   const int* toff = TILE_M == kTileM ? a.tile_off : a.tile_off2;
+  const int ks = a.ksplit > 1 ? a.ksplit : 1;
+  ti.split = t % ks;  // consecutive tiles are the splits of one output tile
+  t /= ks;
   if (a.var_k) {
     const int MT = (a.M + TILE_M - 1) / TILE_M;
     const int gi = t / (MT * NT);
@@ -120,6 +126,13 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int NT
     ti.off = grp_off(a, g);
     ti.kblocks = a.K / kTileK;
   }
+  ti.kb0 = 0;
+  ti.kb_last = ti.kblocks - 1;
+  if (ks > 1) {  // this split's share of the k-blocks
+    const int per = (ti.kblocks + ks - 1) / ks;
+    ti.kb0 = ti.split * per;
+    ti.kblocks = max(0, min(per, ti.kblocks - ti.kb0));
+  }
   return ti;
 }
 
@@ -127,9 +140,10 @@ template <int BN, int TILE_M>
 __device__ __forceinline__ int total_tiles(const GemmArgs& a) {
   const int NT = n_tiles<BN>(a);
   const int* toff = TILE_M == kTileM ? a.tile_off : a.tile_off2;
-  if (a.var_k) return a.G * ((a.M + TILE_M - 1) / TILE_M) * NT;
+  const int ks = a.ksplit > 1 ? a.ksplit : 1;
+  if (a.var_k) return a.G * ((a.M + TILE_M - 1) / TILE_M) * NT * ks;
   const int mt = toff ? toff[a.G] : (a.rows_const + TILE_M - 1) / TILE_M;
-  return mt * NT;
+  return mt * NT * ks;
 }
 
 // ---------------------------------------------------------------- epilogue pieces
@@ -285,7 +299,7 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
     for (int t = cluster_id; t < total && ok; t += num_clusters) {
       const TileInfo ti = decode_tile<BN, C::TILE_M>(args, t, NT, rec);
       if (t + num_clusters < total) rec = load_tile_rec<BN, C::TILE_M>(args, t + num_clusters, NT);
-      for (int kb = 0; kb < ti.kblocks; ++kb) {
+      for (int kb = ti.kb0; kb < ti.kb0 + ti.kblocks; ++kb) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -337,7 +351,7 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
       if (!free_acc) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-      for (int kb = 0; kb < ti.kblocks; ++kb) {
+      for (int kb = ti.kb0; kb < ti.kb0 + ti.kblocks; ++kb) {
         if (!mbar_wait_bounded(&full[stage], phase, abort_flag)) {
           ok = false;
           break;
@@ -346,8 +360,8 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
         // descriptors of this stage: the k16 steps only move the start address
         const uint64_t ad = adesc0 + (uint64_t)(stage * (C::STAGE_BYTES >> 4));
         const uint64_t bd = bdesc0 + (uint64_t)(stage * (C::STAGE_BYTES >> 4));
-        const uint32_t acc0 = kb != 0 ? 1u : 0u;
-        if (!(args.var_k && kb == ti.kblocks - 1)) {  // full k-block: four k16 steps
+        const uint32_t acc0 = kb != ti.kb0 ? 1u : 0u;
+        if (!(args.var_k && kb == ti.kb_last)) {  // full k-block: four k16 steps
           mma(d_tmem, ad, bd, acc0);
           mma(d_tmem, ad + astep, bd + bstep, 1u);
           mma(d_tmem, ad + 2 * astep, bd + 2 * bstep, 1u);
@@ -423,7 +437,8 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
         __syncwarp();
         aux_prefetch(aux_buf, ab_aux, aux_row0, args.ld_aux, args.N, ncol0 + c_begin * 64, rows_left, lane);
       }
-      const bool empty_tile = ti.kblocks == 0;  // variable-K group with no rows: output is zero
+      // variable-K group without rows, or a K split without k-blocks: the output is zero
+      const bool empty_tile = ti.kblocks == 0;
       const int acc = acc_i & 1;
       if (!empty_tile) {
         const uint32_t acc_par = (uint32_t)((acc_i >> 1) & 1);
@@ -461,19 +476,28 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
               tmem_ld_wait(ra);
             }
           }
-          if constexpr (!tma_out) {  // fp32 logits (single group): direct 16-byte stores, one row per thread
+          if constexpr (!tma_out) {  // fp32: direct 16-byte stores, one row per thread
             const int nh = n0 + hh * 32;
-            if (!empty_tile && m < ti.rows && nh < args.N) {
-              float* o = reinterpret_cast<float*>(args.out0) + ((int64_t)ti.off + m) * args.ldo + nh;
+            const bool row_ok = args.var_k ? m < args.M : m < ti.rows;
+            if (row_ok && nh < args.N) {
+              const int64_t orow = args.var_k ? (int64_t)ti.g * args.M + m : (int64_t)ti.off + m;
+              float* o = reinterpret_cast<float*>(args.out0) + ti.split * args.part_stride + orow * args.ldo + nh;
               const int nv = min(32, args.N - nh);
-              if (nv == 32 && (reinterpret_cast<uintptr_t>(o) & 15) == 0) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                  *reinterpret_cast<uint4*>(o + i) = make_uint4(ra[i], ra[i + 1], ra[i + 2], ra[i + 3]);
-              } else {
+              for (int half = 0; half < 2; ++half) {  // the paired second half goes to column N
+                if (half && !args.paired) break;
+                float* oh = o + (half ? args.N : 0);
+                const uint32_t* r = half ? rb : ra;
+                if (nv == 32 && (reinterpret_cast<uintptr_t>(oh) & 15) == 0) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (i < nv) o[i] = __uint_as_float(ra[i]);
+                  for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<uint4*>(oh + i) = empty_tile ? make_uint4(0, 0, 0, 0)
+                                                                   : make_uint4(r[i], r[i + 1], r[i + 2], r[i + 3]);
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 32; ++i)
+                    if (i < nv) oh[i] = empty_tile ? 0.0f : __uint_as_float(r[i]);
+                }
               }
             }
             continue;
@@ -729,6 +753,8 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_s
     case EPI_DW:
       if (need > 2 * kT) return cudaErrorInvalidValue;
       return launch_cfg<256, 6, 2 * kT, EPI_DW, 2>(a, st, num_sms);
+    case EPI_F32:
+      return launch_cfg<256, 4, kT, EPI_F32, 1>(a, st, num_sms);
     default:
       return cudaErrorInvalidValue;
   }
@@ -743,6 +769,8 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_s
     case EPI_STORE:
       if (need > 2 * kT) return cudaErrorInvalidValue;
       return launch_cfg<256, 4, 2 * kT, EPI_STORE, 1>(a, st, num_sms);
+    case EPI_F32:  // fp32 partial sums of a K split (decode-sized expert GEMMs)
+      return launch_cfg<256, 4, kT, EPI_F32, 1>(a, st, num_sms);
     case EPI_DW:  // short-K tiles: the epilogue sets the pace, so eight epilogue warps
       if (need > 2 * kT) return cudaErrorInvalidValue;
       return launch_cfg<256, 3, 2 * kT, EPI_DW, 1, 8>(a, st, num_sms);

@@ -8,8 +8,11 @@
 
 namespace moe {
 
+// part / nsplit / part_stride: the router GEMM's fp32 partial sums when it ran as a
+// K split (null: logits already hold the sums)
 cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, int k, int* topk_idx, float* topk_w,
-                              uint64_t* masks, cudaStream_t st);
+                              uint64_t* masks, cudaStream_t st, const float* part = nullptr, int nsplit = 1,
+                              int64_t part_stride = 0);
 cudaError_t launch_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset, int* pad_off,
                               int* tile_off, int* chunk_base, int* pair_of_row, int* user_offsets, cudaStream_t st,
                               int* order = nullptr, int* tile_off2 = nullptr, int4* tile_rec = nullptr,
@@ -30,6 +33,14 @@ cudaError_t launch_pair_score(const void* dy, const void* y_pair, const int* pai
                               float* score, void* dy_perm, float* user_scores, int num_sms, cudaStream_t st);
 cudaError_t launch_select(const float* score, const int* count, const int* pad_off, const int* quota, int E,
                           int* ret_cidx, int* ret_count, int* status, cudaStream_t st);
+// K-split second pass (splitk.cu): ordered sums of the fp32 partials, then the
+// epilogue of the unsplit GEMM (bf16 store, or the SwiGLU forward into ab and h).
+// Rows: *nrows_dev when given, else nrows_const; max_rows bounds the grid.
+cudaError_t launch_splitk_store(const float* part, int64_t stride, int S, const int* nrows_dev, int nrows_const,
+                                int64_t max_rows, const int* pair_of_row, int N, int64_t ldo, void* out, int num_sms,
+                                cudaStream_t st);
+cudaError_t launch_splitk_swiglu(const float* part, int64_t stride, int S, const int* nrows_dev, int64_t max_rows,
+                                 const int* pair_of_row, int F, void* ab, void* h, int num_sms, cudaStream_t st);
 cudaError_t launch_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off, int* ret_tile_off,
                             int* ret_src, int* user_offsets, cudaStream_t st, int* order = nullptr,
                             int* ret_tile_off2 = nullptr, int4* tile_rec = nullptr, int4* ord_rec = nullptr);

@@ -63,10 +63,13 @@ struct WsPtrs {
   int4* ret_tile_rec;   // same for the kept rows
   int4* ord_rec;        // [E] experts in dW order: {expert, count, pad_off, 0}
   int4* ret_ord_rec;    // same for the kept rows
+  float* part;          // fp32 partial sums of a K-split GEMM, split after split
 };
 
 struct WsLayout {
   int64_t T, H, F, E, k, Fs, P, Rmax, Tpad, C;
+  int64_t Rdec;        // padded permuted rows actually used: T*k + 15*min(E, T*k)
+  int64_t part_elems;  // fp32 elements of the K-split partial buffer (0: no split possible)
   int es;  // bytes per I/O element
   size_t total;
   size_t off[64];

@@ -87,6 +87,18 @@ WsLayout make_layout(const moe_dims* d) {
   L.es = d->dtype == MOE_BF16 ? 2 : 4;
   const int64_t es = L.es, T = L.T, H = L.H, F = L.F, E = L.E, k = L.k, Fs = L.Fs, P = L.P, R = L.Rmax,
                 Tp = L.Tpad, C = L.C;
+  L.Rdec = std::min<int64_t>(R, P + 15 * std::min<int64_t>(E, P));
+  {  // K-split partials: room for kMaxSplit splits of every GEMM that may be split on a GPU of up to
+     // kSplitMaxSms SMs (the split needs at most half the SMs busy without it)
+    auto few = [](int64_t tiles) { return tiles * 2 <= kSplitMaxSms; };
+    const int64_t act = std::min<int64_t>(E, P) + P / 128;  // bound on 128-row expert tiles
+    int64_t per = 0;
+    if (few(((T + 127) / 128) * ((E + 127) / 128))) per = std::max(per, T * E);        // router logits
+    if (few(((H + 127) / 128) * ((E + 127) / 128))) per = std::max(per, H * E);        // router dW
+    if (few(act * ((F + 127) / 128))) per = std::max(per, L.Rdec * 2 * F);            // expert gate/up
+    if (few(act * ((H + 255) / 256))) per = std::max(per, L.Rdec * H);                // expert down
+    L.part_elems = per * kMaxSplit;
+  }
   const int64_t sizes[] = {
       256,                       // status
       T * E * 4,                 // logits
@@ -107,6 +119,7 @@ WsLayout make_layout(const moe_dims* d) {
       (E + 1) * 4, (E + 1) * 4,            // tile_off2 ret_tile_off2
       (P / 128 + E + 1) * 16, (P / 128 + E + 1) * 16,  // tile_rec ret_tile_rec
       E * 16, E * 16,                                  // ord_rec ret_ord_rec
+      L.part_elems * 4,                                // part
   };
   L.n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   size_t off = 0;
@@ -125,7 +138,7 @@ const char* const kEntryNames[] = {
     "sh_y", "g", "score", "dy_perm", "ret_cidx", "ret_count", "ret_offset", "ret_pad_off", "ret_tile_off",
     "ret_src", "crow_of_pair", "ret_rows", "x_c", "ab_c", "h_c", "dy_c", "dab", "dx_pair", "dl", "dl_sel", "wrT",
     "sh_dab", "sh_dx", "order", "ret_order", "tile_off2", "ret_tile_off2", "tile_rec", "ret_tile_rec", "ord_rec",
-    "ret_ord_rec"};
+    "ret_ord_rec", "part"};
 
 WsPtrs make_ptrs(const WsLayout& L, void* ws) {
   char* b = static_cast<char*>(ws);
@@ -183,6 +196,7 @@ WsPtrs make_ptrs(const WsLayout& L, void* ws) {
   p.ret_tile_rec = (int4*)nx();
   p.ord_rec = (int4*)nx();
   p.ret_ord_rec = (int4*)nx();
+  p.part = (float*)nx();
   return p;
 }
 
@@ -285,6 +299,17 @@ cudaError_t run_gemm(const GemmArgs& a, int bf16, int bn, cudaStream_t st, int s
   return launch_simt_gemm_f32(a, st);
 }
 
+// K split of a GEMM with `tiles` output tiles of `kblocks` k-blocks: used only when
+// the tiles alone would leave at least half of the SMs idle, and only as far as the
+// partial buffer holds `elems` fp32 per split. No split is left without k-blocks.
+int ksplit_for(const WsLayout& L, int64_t tiles, int kblocks, int sms, int64_t elems) {
+  if (tiles <= 0 || tiles * 2 > sms || kblocks < 2 || elems <= 0) return 1;
+  int ks = (int)std::min<int64_t>({(int64_t)sms / tiles, (int64_t)kblocks, (int64_t)kMaxSplit, L.part_elems / elems});
+  if (ks < 2) return 1;
+  const int per = (kblocks + ks - 1) / ks;
+  return (kblocks + per - 1) / per;
+}
+
 GemmArgs base_args(int* status) {
   GemmArgs a;
   memset(&a, 0, sizeof(a));
@@ -302,6 +327,7 @@ int expert_forward_gemms(const WsLayout& L, const WsPtrs& p, int bf, int sms, cu
                          const void* ws_down, const void* x) {
   const int T = (int)L.T, H = (int)L.H, F = (int)L.F, E = (int)L.E, Fs = (int)L.Fs;
   const bool shared = L.Fs > 0;
+  const int64_t act_tiles = std::min<int64_t>(L.E, L.P) + L.P / 128;  // bound on 128-row expert tiles
   // expert gate/up with fused SwiGLU
   {
     GemmArgs a = base_args(p.status);
@@ -329,7 +355,20 @@ int expert_forward_gemms(const WsLayout& L, const WsPtrs& p, int bf, int sms, cu
     a.ldo1 = F;
     a.zero_pad = 1;
     a.out_rows = L.Rmax;
-    CKL(run_gemm(a, bf, 256, st, sms));
+    const int ks = bf ? ksplit_for(L, act_tiles * ((F + 127) / 128), H / kTileK, sms, L.Rdec * 2 * F) : 1;
+    if (ks > 1) {  // decode-sized: K split into fp32 partials, then the SwiGLU epilogue in a second pass
+      a.epi = EPI_F32;
+      a.out0 = p.part;
+      a.out1 = nullptr;
+      a.ksplit = ks;
+      a.part_stride = L.Rdec * 2 * F;
+      CKL(run_gemm(a, bf, 256, st, sms));
+      Span sp(st, FAM_BW);
+      CKL(launch_splitk_swiglu(p.part, L.Rdec * 2 * F, ks, p.pad_off + E, L.Rdec, p.pair_of_row, F, p.ab, p.h, sms,
+                               st));
+    } else {
+      CKL(run_gemm(a, bf, 256, st, sms));
+    }
   }
   // expert down
   {
@@ -354,7 +393,19 @@ int expert_forward_gemms(const WsLayout& L, const WsPtrs& p, int bf, int sms, cu
     a.ldo = H;
     a.zero_pad = 1;
     a.out_rows = L.Rmax;
-    CKL(run_gemm(a, bf, 256, st, sms));
+    const int ks = bf ? ksplit_for(L, act_tiles * ((H + 255) / 256), F / kTileK, sms, L.Rdec * H) : 1;
+    if (ks > 1) {
+      a.epi = EPI_F32;
+      a.out0 = p.part;
+      a.ksplit = ks;
+      a.part_stride = L.Rdec * H;
+      CKL(run_gemm(a, bf, 256, st, sms));
+      Span sp(st, FAM_BW);
+      CKL(launch_splitk_store(p.part, L.Rdec * H, ks, p.pad_off + E, 0, L.Rdec, p.pair_of_row, H, H, p.y_pair, sms,
+                              st));
+    } else {
+      CKL(run_gemm(a, bf, 256, st, sms));
+    }
   }
   if (shared) {
     GemmArgs a = base_args(p.status);
@@ -536,6 +587,7 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
   CK(cudaMemsetAsync(p.status, 0, sizeof(int), st));
 
   // router logits = x W_r  (fp32 out; bias added by the top-k kernel)
+  const int rks = bf ? ksplit_for(L, ((L.T + 127) / 128) * ((L.E + 127) / 128), H / kTileK, sms, L.T * L.E) : 1;
   {
     GemmArgs a = base_args(p.status);
     a.var_k = 0;
@@ -552,11 +604,17 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.epi = EPI_F32;
     a.out0 = p.logits;
     a.ldo = E;
+    if (rks > 1) {  // few tiles: K split, the top-k kernel adds the partial sums
+      a.ksplit = rks;
+      a.out0 = p.part;
+      a.part_stride = (int64_t)T * E;
+    }
     CKL(run_gemm(a, bf, 128, st, sms));
   }
   {
     Span sp(st, FAM_BW);
-    CKL(launch_route_topk(p.logits, router_bias, T, E, k, p.topk_idx, p.topk_w, p.masks, st));
+    CKL(launch_route_topk(p.logits, router_bias, T, E, k, p.topk_idx, p.topk_w, p.masks, st,
+                          rks > 1 ? p.part : nullptr, rks, (int64_t)T * E));
     CKL(launch_route_scan(p.masks, (int)L.C, E, p.count, p.offset, p.pad_off, p.tile_off, p.chunk_base, p.pair_of_row,
                          expert_offsets, st, p.order, p.tile_off2, p.tile_rec, p.ord_rec));
     CKL(launch_route_index(p.masks, p.chunk_base, p.topk_idx, p.offset, p.pad_off, T, E, k, p.rowp_of_pair,
@@ -915,7 +973,20 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
       a.epi = EPI_DW;
       a.out0 = dw_router;
       a.ldo = E;
-      CKL(run_gemm(a, bf, 128, st, sms));
+      const int ks = bf ? ksplit_for(L, ((L.H + 127) / 128) * ((L.E + 127) / 128), (T + kTileK - 1) / kTileK, sms,
+                                     L.H * L.E)
+                        : 1;
+      if (ks > 1) {  // few tiles, long K (all tokens): K split, then an ordered sum into bf16
+        a.epi = EPI_F32;
+        a.out0 = p.part;
+        a.ksplit = ks;
+        a.part_stride = L.H * L.E;
+        CKL(run_gemm(a, bf, 128, st, sms));
+        Span sp(st, FAM_BW);
+        CKL(launch_splitk_store(p.part, L.H * L.E, ks, nullptr, H, H, nullptr, E, E, dw_router, sms, st));
+      } else {
+        CKL(run_gemm(a, bf, 128, st, sms));
+      }
     }
     if (shared) {
       GemmArgs a = base_args(p.status);

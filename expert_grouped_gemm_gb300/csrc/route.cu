@@ -23,17 +23,44 @@ constexpr int kChunk = 64;  // tokens per routing chunk (one bit each in a uint6
 // registers. The chunk masks (zeroed by the launcher) get one bit per pair.
 template <int EPL>
 __global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* bias, int T, int E, int k,
-                                                    int* topk_idx, float* topk_w, uint64_t* masks) {
+                                                    int* topk_idx, float* topk_w, uint64_t* masks,
+                                                    const float* part, int nsplit, int64_t part_stride) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
   float* lrow = logits + (int64_t)t * E;
   float v[EPL];
+  float l[EPL];
+  if (part) {  // the router GEMM ran as a K split: its partial sums, added in split order
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) l[i] = 0.0f;
+    for (int s0 = 0; s0 < nsplit; s0 += 4) {
+      float q[4][EPL];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int e = lane + 32 * i;
+          q[j][i] = (s0 + j < nsplit && e < E) ? part[(s0 + j) * part_stride + (int64_t)t * E + e] : 0.0f;
+        }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+          if (s0 + j < nsplit) l[i] += q[j][i];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      l[i] = e < E ? lrow[e] : 0.0f;
+    }
+  }
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
-      const float x = lrow[e] + (bias ? bias[e] : 0.0f);
+      const float x = l[i] + (bias ? bias[e] : 0.0f);
       lrow[e] = x;                     // the biased logits the selection used
       v[i] = (x != x) ? -INFINITY : x;  // NaN ranks last
     }
@@ -334,18 +361,18 @@ __global__ void __launch_bounds__(256, 4) k_combine_k8(const __nv_bfloat16* __re
 
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, int k, int* topk_idx, float* topk_w,
-                              uint64_t* masks, cudaStream_t st) {
+                              uint64_t* masks, cudaStream_t st, const float* part, int nsplit, int64_t part_stride) {
   const int C = (T + kChunk - 1) / kChunk;
   cudaError_t e = cudaMemsetAsync(masks, 0, (size_t)C * E * sizeof(uint64_t), st);
   if (e != cudaSuccess) return e;
   const int grid = (T + 7) / 8;
   const int epl = (E + 31) / 32;
-  if (epl <= 1) k_route_topk<1><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
-  else if (epl <= 2) k_route_topk<2><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
-  else if (epl <= 4) k_route_topk<4><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
-  else if (epl <= 8) k_route_topk<8><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
-  else if (epl <= 16) k_route_topk<16><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
-  else k_route_topk<32><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks);
+  if (epl <= 1) k_route_topk<1><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride);
+  else if (epl <= 2) k_route_topk<2><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride);
+  else if (epl <= 4) k_route_topk<4><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride);
+  else if (epl <= 8) k_route_topk<8><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride);
+  else if (epl <= 16) k_route_topk<16><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride);
+  else k_route_topk<32><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride);
   return cudaGetLastError();
 }
 
