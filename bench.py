@@ -312,37 +312,70 @@ def run_ours(args):
     ms_per_step = ms / args.steps
     value = world * w.T * args.steps / (ms / 1e3)
 
-    # ---- end to end through the public API: pinned host inputs in, results out
+    # ---- end to end through the public API: pinned host inputs in, results out.
+    # Pipelined as a serving loop would run it: step i+1's inputs are copied in on a
+    # second stream while step i computes, and step i's Y and dX are copied out while
+    # step i+1 computes; inputs and outputs are double-buffered, every copy of every
+    # timed step (and the last step's results) is inside the timed region.
     hx = torch.empty_like(inp["x"]).pin_memory()
     hx.copy_(inp["x"])
     hdy = torch.empty_like(inp["dy"]).pin_memory()
     hdy.copy_(inp["dy"])
     hq = inp["quota"].pin_memory() if quota is not None else None
-    hy = torch.empty_like(hx).pin_memory()
-    hdx = torch.empty_like(hx).pin_memory()
-    dx_dev = torch.empty_like(x)
-    dy_dev = torch.empty_like(dy)
-    q_dev = torch.empty_like(quota) if quota is not None else None
+    hy = [torch.empty_like(hx).pin_memory() for _ in range(2)]
+    hdx = [torch.empty_like(hx).pin_memory() for _ in range(2)]
+    x_in = [torch.empty_like(x) for _ in range(2)]
+    dy_in = [torch.empty_like(dy) for _ in range(2)]
+    q_in = [torch.empty_like(quota) for _ in range(2)] if quota is not None else [None, None]
+    y_out = [torch.empty_like(layer.y) for _ in range(2)]
+    dx_out = [torch.empty_like(layer.dx) for _ in range(2)]
+    cstream = torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()
+    in_ready, in_free, out_ready, out_free = [ev(), ev()], [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    for b in range(2):  # nothing is in flight yet
+        in_free[b].record(stream)
+        out_free[b].record(stream)
     e2e_steps = max(1, min(args.steps, 100))
 
-    def e2e_step():
-        dx_dev.copy_(hx, non_blocking=True)
-        dy_dev.copy_(hdy, non_blocking=True)
-        if q_dev is not None:
-            q_dev.copy_(hq, non_blocking=True)
-        layer.step(dx_dev, dy_dev, q_dev)
-        hy.copy_(layer.y, non_blocking=True)
-        hdx.copy_(layer.dx, non_blocking=True)
+    def copy_in(i):
+        b = i % 2
+        with torch.cuda.stream(cstream):
+            cstream.wait_event(in_free[b])
+            x_in[b].copy_(hx, non_blocking=True)
+            dy_in[b].copy_(hdy, non_blocking=True)
+            if q_in[b] is not None:
+                q_in[b].copy_(hq, non_blocking=True)
+            in_ready[b].record(cstream)
 
-    for _ in range(3):
-        e2e_step()
+    def compute_and_copy_out(i, n):
+        b = i % 2
+        stream.wait_event(in_ready[b])
+        stream.wait_event(out_free[b])
+        layer.y, layer.dx = y_out[b], dx_out[b]
+        layer.step(x_in[b], dy_in[b], q_in[b])
+        in_free[b].record(stream)
+        out_ready[b].record(stream)
+        if i + 1 < n:
+            copy_in(i + 1)
+        with torch.cuda.stream(cstream):
+            cstream.wait_event(out_ready[b])
+            hy[b].copy_(y_out[b], non_blocking=True)
+            hdx[b].copy_(dx_out[b], non_blocking=True)
+            out_free[b].record(cstream)
+
+    def run_e2e(n):
+        copy_in(0)
+        for i in range(n):
+            compute_and_copy_out(i, n)
+        stream.wait_stream(cstream)
+
+    run_e2e(3)
     barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    run_e2e(e2e_steps)
     e1.record(stream)
     torch.cuda.synchronize()
     ems = e0.elapsed_time(e1)
@@ -353,7 +386,7 @@ def run_ours(args):
     e2e_value = world * w.T * e2e_steps / (ems / 1e3)
     h2d = hx.numel() * hx.element_size() + hdy.numel() * hdy.element_size() + (
         hq.numel() * hq.element_size() if hq is not None else 0)
-    d2h = hy.numel() * hy.element_size() + hdx.numel() * hdx.element_size()
+    d2h = hy[0].numel() * hy[0].element_size() + hdx[0].numel() * hdx[0].element_size()
 
     if world > 1:
         torch.distributed.barrier()
@@ -392,7 +425,8 @@ def run_ours(args):
                              f"{3 * w.E * w.H * w.F * 2 / 1e9:.2f} GB, read twice per step)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "gpu_launches": int(n1 - n0), "clocks": clk,
-            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "copies": "pinned host buffers; on a second stream, overlapped with the neighbouring steps"},
             "roofline": roof}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, args.seed, args.cpu_budget_s)
