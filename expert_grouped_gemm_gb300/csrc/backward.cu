@@ -468,7 +468,7 @@ cudaError_t launch_transpose(const void* in, int R, int Cc, void* out, cudaStrea
 // bf16, k <= 8: persistent blocks; the next token's slot metadata is loaded by k
 // threads while this token's rows are in flight and handed over through shared
 // memory at the token boundary. Same summation order as k_dx_reduce.
-__global__ void __launch_bounds__(256, 3) k_dx_reduce_k8(const __nv_bfloat16* __restrict__ dx_pair,
+__global__ void __launch_bounds__(256, 2) k_dx_reduce_k8(const __nv_bfloat16* __restrict__ dx_pair,
                                                       const int* __restrict__ crow_of_pair,
                                                       const int* __restrict__ topk_idx, const float* __restrict__ dl_sel,
                                                       const __nv_bfloat16* __restrict__ wrT,
@@ -495,11 +495,12 @@ __global__ void __launch_bounds__(256, 3) k_dx_reduce_k8(const __nv_bfloat16* __
       d_next = dl_sel[(int64_t)tn * k + tid];
     }
     for (int i = tid; i < H / 8; i += blockDim.x) {
-      uint4 u[8];
+      uint4 u[8], v[8];  // the slots' dx_pair rows and router-weight rows, all loads in flight together
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int cr = s_c[buf][j];
         u[j] = cr >= 0 ? reinterpret_cast<const uint4*>(dx_pair + (int64_t)cr * H)[i] : make_uint4(0, 0, 0, 0);
+        if (j < k) v[j] = reinterpret_cast<const uint4*>(wrT + (int64_t)s_e[buf][j] * H)[i];
       }
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, f[8];
 #pragma unroll
@@ -511,12 +512,9 @@ __global__ void __launch_bounds__(256, 3) k_dx_reduce_k8(const __nv_bfloat16* __
         }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < k) u[j] = reinterpret_cast<const uint4*>(wrT + (int64_t)s_e[buf][j] * H)[i];
-#pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (j < k) {
-          bf16x8_to_f(u[j], f);
+          bf16x8_to_f(v[j], f);
           const float d = s_d[buf][j];
 #pragma unroll
           for (int q = 0; q < 8; ++q) acc[q] = fmaf(d, f[q], acc[q]);

@@ -72,6 +72,47 @@ __global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* 
   float lmax = 0.0f, sum = 0.0f;
   uint64_t* cmask = masks + (int64_t)(t / kChunk) * E;
   const uint64_t bit = 1ull << (t % kChunk);
+  if (k <= 32) {
+    // every lane sees each round's winner; lane j keeps slot j's expert and weight and
+    // writes them itself, so no lane walks the k slots and nothing is read back
+    int my_e = 0;
+    float my_w = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (!((taken >> i) & 1u) && (be == 0x7fffffff || v[i] > bv)) {  // e ascending: ties keep the first
+          bv = v[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (j == 0) lmax = bv;
+      const float ex = expf(bv - lmax);
+      sum += ex;  // the same order on every lane: slot 0 first
+      if (lane == j) {
+        my_e = be;
+        my_w = ex;
+      }
+    }
+    if (lane < k) {
+      topk_idx[(int64_t)t * k + lane] = my_e;
+      topk_w[(int64_t)t * k + lane] = my_w * (1.0f / sum);
+      atomicOr(reinterpret_cast<unsigned long long*>(&cmask[my_e]), bit);
+    }
+    return;
+  }
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
     int be = 0x7fffffff;
