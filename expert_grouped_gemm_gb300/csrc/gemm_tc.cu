@@ -395,8 +395,12 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
     constexpr bool tma_out = EPI != EPI_F32;
     constexpr bool bwd = EPI == EPI_SWIGLU_BWD;
     constexpr bool fwd = EPI == EPI_SWIGLU_FWD;
+    // dW of a pair of weights (gate and up) with one staging tile per warp: dW_up goes
+    // out through the tile after dW_gate's store has read it
+    constexpr bool serial_pair = EPI == EPI_DW && EPI_WARP_BYTES < 2 * kStageTileBytes;
+    const bool pair_later = serial_pair && args.paired;
     // staged outputs per chunk (the SwiGLU forward stages a|b, then h in the a tile)
-    const int nout = (fwd || bwd || (EPI == EPI_DW && args.paired)) ? 2 : 1;
+    const int nout = (fwd || bwd || (EPI == EPI_DW && args.paired && !serial_pair)) ? 2 : 1;
     // one output alternates two staging sets when room allows; otherwise one set
     const int nbuf = (nout == 1 && EPI_WARP_BYTES >= 2 * kStageTileBytes) ? 2 : 1;
     // SwiGLU bwd: the a and b tiles of one chunk; da and db are staged in place over them
@@ -538,6 +542,7 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
               if (!store) continue;
               st_shared_v4(set + stage_off(lane, j), f_to_bf16x8(x0));
               if (nout > 1) st_shared_v4(set + kStageTileBytes + stage_off(lane, j), f_to_bf16x8(x1));
+              else if (pair_later) hpk[j] = f_to_bf16x8(x1);
             }
           }
         }
@@ -568,7 +573,7 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
           __syncwarp();
           aux_prefetch(aux_buf, ab_aux, aux_row0, args.ld_aux, args.N, n0 + 64, rows_left, lane);
         }
-        if (fwd) {  // h goes out through the a tile once a|b have been read from it
+        if (fwd || pair_later) {  // h (dW_up) goes out through the a (dW_gate) tile once it has been read
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
 #pragma unroll
@@ -726,7 +731,8 @@ static int staging_bytes(const GemmArgs& a) {
   if (a.epi == EPI_F32) return 0;
   if (a.epi == EPI_SWIGLU_FWD) return 2 * kStageTileBytes;
   if (a.epi == EPI_SWIGLU_BWD) return 2 * kStageTileBytes;  // a|b tiles, da|db staged in place
-  return ((a.epi == EPI_DW && a.paired) ? 2 : 1) * kStageTileBytes;
+  if (a.epi == EPI_DW && a.paired && MOE_GEMM_CTAS == 2) return 2 * kStageTileBytes;  // pair build: both staged
+  return kStageTileBytes;
 }
 
 cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_sms, int /*max_tiles_hint*/) {
@@ -771,9 +777,9 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_s
       return launch_cfg<256, 4, 2 * kT, EPI_STORE, 1>(a, st, num_sms);
     case EPI_F32:  // fp32 partial sums of a K split (decode-sized expert GEMMs)
       return launch_cfg<256, 4, kT, EPI_F32, 1>(a, st, num_sms);
-    case EPI_DW:  // short-K tiles: the epilogue sets the pace, so eight epilogue warps
-      if (need > 2 * kT) return cudaErrorInvalidValue;
-      return launch_cfg<256, 3, 2 * kT, EPI_DW, 1, 8>(a, st, num_sms);
+    case EPI_DW:  // short-K tiles: the epilogue sets the pace, so eight epilogue warps (4 KB staging each)
+      if (need > kT) return cudaErrorInvalidValue;
+      return launch_cfg<256, 4, kT, EPI_DW, 1, 8>(a, st, num_sms);
     default:
       return cudaErrorInvalidValue;
   }
