@@ -40,17 +40,31 @@ __global__ void __launch_bounds__(256) k_pair_score(const TIO* dy, const TIO* y_
     TIO* dst = dy_perm ? dy_perm + (int64_t)r * H : nullptr;
     float ss = 0.0f, dot = 0.0f;
     if constexpr (sizeof(TIO) == 2) {
-      for (int i = lane; i < H / 8; i += 32) {
-        float a[8], b[8];
-        bf16x8_to_f(reinterpret_cast<const uint4*>(dyr)[i], a);
-        bf16x8_to_f(reinterpret_cast<const uint4*>(yr)[i], b);
+      const int nv = H / 8;
+      for (int i0 = lane; i0 < nv; i0 += 32 * 4) {  // four column groups' loads in flight per lane
+        uint4 ua[4], ub[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          ss = fmaf(a[q], a[q], ss);
-          dot = fmaf(a[q], b[q], dot);
-          a[q] *= w;
+        for (int j = 0; j < 4; ++j) {
+          if (i0 + 32 * j < nv) {
+            ua[j] = reinterpret_cast<const uint4*>(dyr)[i0 + 32 * j];
+            ub[j] = reinterpret_cast<const uint4*>(yr)[i0 + 32 * j];
+          }
         }
-        if (dst) reinterpret_cast<uint4*>(dst)[i] = f_to_bf16x8(a);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (i0 + 32 * j < nv) {
+            float a[8], b[8];
+            bf16x8_to_f(ua[j], a);
+            bf16x8_to_f(ub[j], b);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              ss = fmaf(a[q], a[q], ss);
+              dot = fmaf(a[q], b[q], dot);
+              a[q] *= w;
+            }
+            if (dst) reinterpret_cast<uint4*>(dst)[i0 + 32 * j] = f_to_bf16x8(a);
+          }
+        }
       }
     } else {
       for (int i = lane; i < H; i += 32) {

@@ -259,13 +259,21 @@ __global__ void __launch_bounds__(256) k_gather_rows(const TIO* x, const int* pa
         for (int i = lane; i < nv; i += 32) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
       } else {
         const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)(p / k) * H);
-        for (int i = lane; i < nv; i += 32) {
-          const uint4 u = src[i];
-          reinterpret_cast<uint4*>(dst)[i] = u;
-          float f[8];
-          bf16x8_to_f(u, f);
+        for (int i0 = lane; i0 < nv; i0 += 32 * 8) {  // eight loads in flight per lane, then their stores
+          uint4 u[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
+          for (int j = 0; j < 8; ++j)
+            if (i0 + 32 * j < nv) u[j] = src[i0 + 32 * j];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (i0 + 32 * j < nv) {
+              reinterpret_cast<uint4*>(dst)[i0 + 32 * j] = u[j];
+              float f[8];
+              bf16x8_to_f(u[j], f);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
+            }
+          }
         }
       }
     } else {
