@@ -73,6 +73,26 @@ def test_workspace_entries_cover_the_size(lib):
     assert {"ab", "h", "y_pair", "pad_off", "x_perm"} <= set(ents)
 
 
+def _part_bytes(**kw):
+    return _lib.moe_workspace_entries(_dims(**kw))["part"][1]
+
+
+def test_workspace_holds_k_split_partials(lib):
+    """The fp32 partial buffer of a K-split GEMM: room for 16 splits of the largest GEMM that
+    can have too few tiles for the GPU (up to 256 SMs: at most 128 tiles), and none otherwise."""
+    fp = 16 * 4  # splits x bytes per fp32
+    # decode-sized: router logits, router dW and both expert forward GEMMs can be split;
+    # the largest is the expert gate/up over T*k + 15 min(E, T*k) padded rows
+    T, k, H, F, E = 1, 8, 2048, 768, 128
+    rdec = T * k + 15 * min(E, T * k)
+    assert _part_bytes(T=T, H=H, F=F, E=E, k=k) >= fp * max(rdec * 2 * F, rdec * H, T * E, H * E)
+    # training-sized (T=4096): the expert GEMMs have plenty of tiles, the router GEMMs do not
+    T = 4096
+    assert _part_bytes(T=T, H=H, F=F, E=E, k=k) == (fp * max(T * E, H * E) + 255) // 256 * 256
+    # so many router tiles (T=65536 -> 512 x 1) that no GEMM is ever split, except the router dW
+    assert _part_bytes(T=65536, H=H, F=F, E=E, k=k) == (fp * H * E + 255) // 256 * 256
+
+
 FAKE = ctypes.c_void_p(0x10000)   # host-side checks never dereference pointers
 
 
