@@ -75,21 +75,26 @@ def gemm_flops(w, R: int) -> float:
     return f
 
 
-def gemm_bytes(w, R: int) -> float:
+def gemm_bytes(w, R: int, e_fwd: int | None = None, e_bwd: int | None = None) -> float:
     """Algorithmic DRAM bytes of the grouped GEMMs of one step: every operand read
-    once, every output written once (I/O element size; fp32 router logits)."""
+    once, every output written once (I/O element size; fp32 router logits). Expert
+    weights count only for the experts a GEMM touches: e_fwd experts with routed rows
+    (forward, dH, dX), e_bwd with kept rows (dW: every expert's dW is written, but
+    only e_bwd have rows to read); both default to all E."""
     es = 2 if w.dtype == "bf16" else 4
     T, H, F, E, P, Fs = w.T, w.H, w.F, w.E, w.P, w.F_shared
+    Ef = E if e_fwd is None else e_fwd
+    Eb = E if e_bwd is None else e_bwd
     b = es * (T * H + H * E) + 4 * T * E                                  # router logits
-    b += es * (P * H + 2 * E * H * F + 3 * P * F)                         # gate/up -> a|b, h
-    b += es * (P * F + E * F * H + P * H)                                 # down -> y_pair
-    b += es * (R * H + E * F * H + 4 * R * F)                             # dH (reads a|b, writes da|db)
-    b += es * (2 * R * F + 2 * E * H * F + R * H)                         # dX_pair
+    b += es * (P * H + 2 * Ef * H * F + 3 * P * F)                        # gate/up -> a|b, h
+    b += es * (P * F + Ef * F * H + P * H)                                # down -> y_pair
+    b += es * (R * H + Eb * F * H + 4 * R * F)                            # dH (reads a|b, writes da|db)
+    b += es * (2 * R * F + 2 * Eb * H * F + R * H)                        # dX_pair
     if Fs:
         b += es * (T * H + 2 * H * Fs + 3 * T * Fs) + es * (T * Fs + Fs * H + T * H)
         b += es * (T * H + Fs * H + 4 * T * Fs) + es * (2 * T * Fs + 2 * H * Fs + T * H)
     if not w.frozen:
-        b += es * (R * H + 2 * R * F + 2 * E * H * F)                     # dW gate/up
+        b += es * (R * H + 2 * R * F + 2 * E * H * F)                     # dW gate/up (all E written)
         b += es * (R * F + R * H + E * F * H)                             # dW down
         b += es * (T * H + T * E + H * E)                                 # dW router
         if Fs:
@@ -274,6 +279,8 @@ def run_ours(args):
         raise RuntimeError("device status not OK after warm-up")
     R = int(layer.ret_offsets[-1].item()) if quota is not None else w.P
     counts = torch.diff(layer.offsets).cpu()
+    kept = torch.diff(layer.ret_offsets).cpu() if quota is not None else counts
+    e_fwd, e_bwd = int((counts > 0).sum()), int((kept > 0).sum())
     layer.record = False  # a training step asks for no optional routing outputs
 
     # ---- timed region: K steps, inputs resident in HBM
@@ -399,7 +406,7 @@ def run_ours(args):
     flops = gemm_flops(w, R)
     achieved = flops / (gemm_ms_step / 1e3) / 1e12
     peak = float(peaks["bf16_tflops"])
-    gbytes = gemm_bytes(w, R)
+    gbytes = gemm_bytes(w, R, e_fwd, e_bwd)
     hbm_ach = gbytes / (gemm_ms_step / 1e3) / 1e9
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": None, "kernel": "tc_grouped_gemm (all grouped-GEMM launches of one step)",
