@@ -18,6 +18,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -188,6 +189,18 @@ def oracle_inputs64(w, seed):
     return {k: (None if v is None else bf16_bits_to_f64(v)) for k, v in raw.items() if k != "quota"}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), else the machine architecture."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
 def cpu_baseline(w, seed, budget_s):
     """Oracle tokens/s on a bounded token sample sized to roughly budget_s of CPU work."""
     inp64 = oracle_inputs64(w, seed)
@@ -198,7 +211,7 @@ def cpu_baseline(w, seed, budget_s):
         n = max(16, n - n % 16)
         t = oracle_sample_time(w, inp64, n)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return {"value": n / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+    return {"value": n / t, "unit": "tokens/s", "cores": cores, "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"first {n} of {w.T} tokens of the same layer (all {w.E} experts, same weights), "
                       f"fwd+bwd in numpy fp64, {t:.1f} s"}
 
@@ -227,7 +240,8 @@ def run_reference(args):
             "steps": steps, "warmup": warm, "ms_per_step": 1000.0 * tot / steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, **{k: v for k, v in describe(w).items() if k != "name"}},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "cpu_model": cpu_model(),
+                             "kind": "oracle",
                              "sample": f"{n} of {w.T} tokens per step, numpy fp64 oracle fwd+bwd"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
