@@ -32,7 +32,7 @@ DEFAULT_WORKLOAD = "qwen3_t4096_full"
 METRIC = "MoE layer fwd+bwd tokens/s (1 GB300); grouped-GEMM % of BF16 tensor peak"
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="oracle time budget for cpu_baseline")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -50,6 +50,22 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time; every rank calls it (one process per GPU, any backend)."""
+    if world <= 1:
+        return ms
+    import torch
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_rank_step: int, steps: int, ms: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time (weak scaling)."""
+    return world * tokens_per_rank_step * steps / (ms / 1e3)
 
 
 def load_peaks():
@@ -326,12 +342,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     _lib.moe_timing_enable(False)
     fam_ms, fam_n = _lib.moe_timing_read()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     ms_per_step = ms / args.steps
-    value = world * w.T * args.steps / (ms / 1e3)
+    value = job_throughput(world, w.T, args.steps, ms)
 
     # ---- end to end through the public API: pinned host inputs in, results out.
     # Pipelined as a serving loop would run it: step i+1's inputs are copied in on a
@@ -400,11 +413,8 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     ems = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ems], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ems = float(t.item())
-    e2e_value = world * w.T * e2e_steps / (ems / 1e3)
+    ems = max_over_ranks(ems, world, dev)
+    e2e_value = job_throughput(world, w.T, e2e_steps, ems)
     h2d = hx.numel() * hx.element_size() + hdy.numel() * hdy.element_size() + (
         hq.numel() * hq.element_size() if hq is not None else 0)
     d2h = hy[0].numel() * hy[0].element_size() + hdx[0].numel() * hdx[0].element_size()
