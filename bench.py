@@ -468,11 +468,18 @@ def run_ours(args):
 
 
 def kernel_hash() -> str:
+    """Hash of the grouped-GEMM sources with comments and blank space removed: the key
+    under which DRAM-traffic captures are kept (a comment edit does not invalidate them)."""
     import hashlib
+    import re
 
     h = hashlib.sha256()
     for name in ("gemm_tc.cu", "epilogue.cuh", "common.cuh", "gemm.h"):
-        h.update(open(os.path.join(ROOT, "expert_grouped_gemm_gb300", "csrc", name), "rb").read())
+        src = open(os.path.join(ROOT, "expert_grouped_gemm_gb300", "csrc", name), encoding="utf-8").read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        src = "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+        h.update(src.encode())
     return h.hexdigest()[:16]
 
 

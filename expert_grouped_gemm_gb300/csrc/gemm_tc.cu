@@ -1,6 +1,6 @@
 // gemm_tc.cu -- persistent grouped GEMM on the 5th-generation tensor cores (sm_103a).
 //
-// Per CTA (192 threads, one CTA per SM):
+// Per CTA (64 + 32 * NEPI threads, one CTA per SM):
 //   warp 0      TMA producer: loads A/B k-blocks of 64 into a STAGES-deep
 //               ring of 128-byte-swizzled shared-memory tiles. An MN-major
 //               operand (row-major [K, MN]) is read through a 3-D view
@@ -8,17 +8,19 @@
 //               fills all of its 64-column chunks.
 //   warp 1      MMA issuer: tcgen05.mma (M=128, N=BN, K=16) into one of two
 //               tensor-memory accumulators, commits free smem slots back.
-//   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (one row per
-//               thread), fused epilogue (SwiGLU fwd/bwd, store, dW), then the
-//               results go through a 128-byte-swizzled staging tile in shared
-//               memory and out with TMA bulk tensor stores of 32 rows x 64
-//               columns (16 rows at a group's padded end, which is a multiple
-//               of 16, so a store never reaches into another group's rows).
-// Tiles (group, m-block, n-block) come from device-side group offsets, so the
-// host never learns the per-group row counts. Variable-K groups are visited
-// heaviest first. Every barrier wait is bounded; a wait that runs out sets
-// MOE_ERR_TIMEOUT in the status word, the CTA drains its own copies and MMAs,
-// frees its tensor memory and returns.
+//   warps 2..    NEPI epilogue warps (4, or 8 with two per TMEM lane quarter):
+//               tcgen05.ld of the finished accumulator (one row per thread),
+//               fused epilogue (SwiGLU fwd/bwd, store, dW), then the results
+//               go through a 128-byte-swizzled staging tile in shared memory
+//               and out with TMA bulk tensor stores of 32 rows x 64 columns (16
+//               rows at a group's padded end, which is a multiple of 16, so a
+//               store never reaches into another group's rows); or, for fp32
+//               outputs (router logits, K-split partial sums), direct stores.
+// Tiles (group, m-block, n-block, K split) come from device-side group offsets
+// and per-tile records, so the host never learns the per-group row counts.
+// Variable-K groups are visited heaviest first. Every barrier wait is bounded;
+// a wait that runs out sets MOE_ERR_TIMEOUT in the status word, the CTA drains
+// its own copies and MMAs, frees its tensor memory and returns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
