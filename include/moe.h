@@ -52,7 +52,7 @@ extern "C" {
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = -1,  /* bad dims, null required pointer, misaligned buffer */
-  MOE_ERR_UNSUPPORTED = -2,  /* valid but not supported by this build (e.g. H % 64 != 0 in bf16) */
+  MOE_ERR_UNSUPPORTED = -2,  /* valid but not supported by this library (e.g. H % 64 != 0 in bf16) */
   MOE_ERR_CUDA = -3,         /* a CUDA runtime/driver call failed */
   MOE_ERR_WORKSPACE = -4,    /* workspace null, too small or misaligned */
   MOE_ERR_STATE = -5,        /* call order violated (bwd before fwd, x differs from fwd's x, ...) */
