@@ -149,3 +149,22 @@ def test_full_bwd_requires_gradient_pointers(lib):
     rc = lib.moe_bwd(ctypes.byref(d), FAKE, nbytes, None, FAKE, FAKE, 0, FAKE, None, FAKE, FAKE, FAKE, None, None,
                      None)
     assert rc == _lib.MOE_ERR_INVALID_ARG, _lib.moe_last_error()
+
+
+def test_cta_pair_variant_compiles():
+    """The CTA-pair (cta_group::2) grouped GEMM, kept as a build option, still compiles for sm_103a."""
+    import shutil
+    import subprocess
+
+    from expert_grouped_gemm_gb300 import build as b
+
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    src = os.path.join(b.CSRC, "gemm_tc.cu")
+    os.makedirs(b.BUILD, exist_ok=True)  # in-tree build folder (ignored by git)
+    obj = os.path.join(b.BUILD, "gemm_tc_pair_check.o")
+    r = subprocess.run([nvcc, *b.ARCH, *b.FLAGS, "-DMOE_GEMM_CTAS=2", "-c", src, "-o", obj], capture_output=True,
+                       text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
+    os.remove(obj)
