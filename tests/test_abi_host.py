@@ -168,3 +168,22 @@ def test_cta_pair_variant_compiles():
                        text=True)
     assert r.returncode == 0, r.stderr[-2000:]
     os.remove(obj)
+
+
+def test_binding_refuses_host_tensors_no_cpu_fallback(lib):
+    """Every step of the path runs in the library's kernels: the binding hands only device
+    pointers across and refuses host tensors outright instead of computing on the CPU."""
+    import torch
+
+    d = _dims()
+    T, H, F, E = 128, 256, 128, 16
+    bf = torch.bfloat16
+    cpu = dict(ws=torch.zeros(_lib.moe_workspace_size(d), dtype=torch.uint8), x=torch.zeros(T, H, dtype=bf),
+               w_router=torch.zeros(H, E, dtype=bf), w_gate=torch.zeros(E, H, F, dtype=bf),
+               w_up=torch.zeros(E, H, F, dtype=bf), w_down=torch.zeros(E, F, H, dtype=bf),
+               y=torch.zeros(T, H, dtype=bf))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        _lib.moe_fwd(d, cpu["ws"], cpu["x"], cpu["w_router"], None, cpu["w_gate"], cpu["w_up"], cpu["w_down"],
+                     None, None, None, cpu["y"])
+    with pytest.raises(ValueError, match="required"):
+        _lib._ptr(None, "x")
