@@ -59,6 +59,7 @@ __all__ = [
     "shared_forward",
     "forward",
     "pair_scores",
+    "plan_quota",
     "select_retained",
     "backward",
     "sigmoid",
@@ -268,6 +269,37 @@ def pair_scores(dy, x, w, y_pair, row_of_pair):
             g[r] = float(dy[t] @ y_pair[r])
             score[r] = w[t, j] * dyn[t] * xn[t]
     return g, score
+
+
+def plan_quota(count, rho_num, rho_den, budget=None):
+    """Per-expert retention quotas planned from the forward's routing.
+
+    ([LRMoE] Abstract: the forward plans retention quotas under resource
+    constraints.) The pages give no formula; the reading used is a fraction
+    rho = rho_num / rho_den of the mean load, rounded up, capped at the
+    expert's own load and, when a per-expert budget is given, at that budget
+    (a negative budget counts as zero):
+
+        mean = (sum_e count_e) / E
+        quota_e = min(count_e, ceil(rho * mean) [, max(budget_e, 0)])
+
+    Computed in exact rational arithmetic (Python integers), so the rounding
+    of the ceiling is the mathematical one.
+    """
+    from fractions import Fraction
+
+    count = [int(c) for c in count]
+    E = len(count)
+    pairs = sum(count)
+    cap = Fraction(int(rho_num), int(rho_den)) * Fraction(pairs, E)
+    cap_int = -((-cap.numerator) // cap.denominator)          # ceil of a non-negative rational
+    out = []
+    for e in range(E):
+        q = min(count[e], cap_int)
+        if budget is not None:
+            q = min(q, max(int(budget[e]), 0))
+        out.append(q)
+    return np.asarray(out, dtype=np.int64)
 
 
 def select_retained(score, offset, pair_of_row, k, quota=None):

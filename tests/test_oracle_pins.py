@@ -413,3 +413,81 @@ def test_pair_scores_closed_form():
     # row 1 <- (t1,j1): g = -2;                     score = .5*2*10
     assert g.tolist() == [7.0, -2.0, 1.5, 6.0]
     assert score.tolist() == [1.25, 10.0, 3.75, 10.0]
+
+
+# ---------------------------------------------------------------- quota planner
+
+def test_plan_quota_golden():
+    g = json.load(open(os.path.join(GOLDEN, "plan_quota.json")))
+    for c in g["cases"]:
+        q = O.plan_quota(np.array(c["count"]), c["rho"][0], c["rho"][1],
+                         None if c["budget"] is None else np.array(c["budget"]))
+        assert q.tolist() == c["quota"], c
+
+
+def test_plan_quota_cap_is_the_least_integer_above_the_scaled_mean():
+    """Brute force: the cap is the smallest integer c with c * E * den >= num * pairs
+    (found by counting up, not by a ceiling formula); every quota is the minimum of
+    the load, that cap and the clamped budget."""
+    rng = np.random.default_rng(21)
+    for _ in range(200):
+        E = int(rng.integers(1, 12))
+        count = rng.integers(0, 60, E)
+        num, den = int(rng.integers(0, 9)), int(rng.integers(1, 9))
+        budget = rng.integers(-3, 40, E) if rng.random() < 0.5 else None
+        q = O.plan_quota(count, num, den, budget)
+        pairs = int(count.sum())
+        c = 0
+        while c * E * den < num * pairs:
+            c += 1
+        for e in range(E):
+            want = min(int(count[e]), c)
+            if budget is not None:
+                want = min(want, max(int(budget[e]), 0))
+            assert q[e] == want
+        assert np.all(q >= 0) and np.all(q <= count)
+
+
+def test_plan_quota_large_rho_keeps_every_pair():
+    count = np.array([5, 0, 17, 3])
+    q = O.plan_quota(count, 1 << 20, 1)
+    assert q.tolist() == count.tolist()
+
+
+# ---------------------------------------------------------------- shared expert
+
+def test_torch_autograd_restatement_with_shared_expert():
+    """The shared expert computed independently with torch.nn.functional and added
+    after the routed sum: a gate/up swap, a missing silu or a wrong transpose in the
+    oracle's shared path (forward or backward) fails here."""
+    from expert_grouped_gemm_gb300.inputs import custom, make_inputs, bf16_bits_to_f64
+    w = custom("tiny_shared_f32", T=24, H=16, F=24, E=6, k=2, F_shared=20, dtype="f32", zipf_s=0.7)
+    raw = make_inputs(w, seed=3)
+    inp = {k_: (None if v is None else bf16_bits_to_f64(v)) for k_, v in raw.items()}
+    f = O.forward(inp, w.k)
+    b = O.backward(inp, f, inp["dy"])
+    tx = torch.tensor(inp["x"], requires_grad=True)
+    tr = torch.tensor(inp["w_router"], requires_grad=True)
+    tg = torch.tensor(inp["w_gate"], requires_grad=True)
+    tu = torch.tensor(inp["w_up"], requires_grad=True)
+    td = torch.tensor(inp["w_down"], requires_grad=True)
+    sg = torch.tensor(inp["ws_gate"], requires_grad=True)
+    su = torch.tensor(inp["ws_up"], requires_grad=True)
+    sd = torch.tensor(inp["ws_down"], requires_grad=True)
+    logits = tx @ tr + torch.tensor(inp["router_bias"])
+    idx = torch.tensor(f["idx"])
+    rows = []
+    for t in range(w.T):
+        wt = torch.softmax(logits[t, idx[t]], dim=0)
+        acc = torch.zeros(w.H, dtype=torch.float64)
+        for j in range(w.k):
+            e = int(idx[t, j])
+            acc = acc + wt[j] * _torch_dense_swiglu(tx[t:t + 1], tg[e], tu[e], td[e])[0]
+        rows.append(acc)
+    Y = torch.stack(rows) + _torch_dense_swiglu(tx, sg, su, sd)
+    np.testing.assert_allclose(f["Y"], Y.detach().numpy(), rtol=1e-12, atol=1e-15)
+    (Y * torch.tensor(inp["dy"])).sum().backward()
+    for mine, theirs in [(b["dX"], tx.grad), (b["dw_router"], tr.grad), (b["dw_gate"], tg.grad),
+                         (b["dw_up"], tu.grad), (b["dw_down"], td.grad), (b["dws_gate"], sg.grad),
+                         (b["dws_up"], su.grad), (b["dws_down"], sd.grad)]:
+        np.testing.assert_allclose(mine, theirs.numpy(), rtol=1e-10, atol=1e-14)
