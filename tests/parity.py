@@ -139,3 +139,51 @@ def parity_case(w: Workload, seed: int = 0, inp: dict | None = None):
     fwd, bwd = run_oracle_replay(w, inp, g)
     rep = check_parity(w, g, fwd, bwd, inp)
     return rep, g, layer, inp
+
+
+def run_gpu_planned(w: Workload, inp: dict, rho: tuple[int, int], budget=None, layer: MoELayer | None = None):
+    """fwd, device-planned quota (moe_plan_quota), select with it, bwd; CPU numpy results
+    plus the planned quota."""
+    dev = torch.device("cuda")
+    if layer is None:
+        layer = MoELayer(w, inp, dev, record_routing=True)
+    x = inp["x"].to(dev)
+    dy = inp["dy"].to(dev)
+    layer.forward(x)
+    quota = torch.empty(w.E, dtype=torch.int32, device=dev)
+    bud = None if budget is None else torch.as_tensor(budget, dtype=torch.int32).to(dev)
+    _lib.moe_plan_quota(layer.dims, layer.ws, rho[0], rho[1], quota, budget=bud)
+    layer.select(dy, quota)
+    dx, grads = layer.backward(dy, x, True)
+    status = _lib.moe_read_status(layer.ws)
+    torch.cuda.synchronize()
+    f = lambda t: t.detach().float().cpu().numpy().astype(np.float64)
+    out = dict(status=status, Y=f(layer.y), dX=f(dx), idx=layer.topk_idx.cpu().numpy().astype(np.int64),
+               w=layer.topk_w.cpu().numpy().astype(np.float64), offsets=layer.offsets.cpu().numpy().astype(np.int64),
+               row_of_pair=layer.row_of_pair.cpu().numpy().astype(np.int64), logits=layer.logits.cpu().numpy(),
+               used_quota=True, quota=quota.cpu().numpy().astype(np.int64))
+    out["ret_offsets"] = layer.ret_offsets.cpu().numpy().astype(np.int64)
+    out["ret_rows"] = layer.ret_rows[:int(out["ret_offsets"][-1])].cpu().numpy().astype(np.int64)
+    out["scores"] = layer.scores.cpu().numpy()
+    for n, t in grads.items():
+        out[n] = f(t)
+    return out, layer
+
+
+def planned_parity_case(w: Workload, rho: tuple[int, int], budget=None, seed: int = 0):
+    """Parity of the device quota planner and the retained backward it drives: the
+    oracle plans its own quota (oracle.plan_quota) from the replayed routing's counts,
+    the planned quotas must be equal, then the select + backward are compared as in
+    every other parity case."""
+    inp = make_inputs(w, seed)
+    g, layer = run_gpu_planned(w, inp, rho, budget)
+    i64 = oracle_inputs(inp)
+    fwd = O.forward(i64, w.k, logits_override=g["logits"])
+    q_or = O.plan_quota(fwd["count"], rho[0], rho[1], None if budget is None else np.asarray(budget))
+    assert np.array_equal(g["quota"], q_or), "planned quotas differ from the oracle's"
+    score_rows = np.empty(w.P, dtype=np.float32)
+    score_rows[fwd["row_of_pair"]] = g["scores"]
+    bwd = O.backward(i64, fwd, i64["dy"], quota=q_or, frozen=w.frozen, score_override=score_rows)
+    rep = check_parity(w, g, fwd, bwd, inp)
+    rep["quota_sum"] = int(q_or.sum())
+    return rep, g, layer

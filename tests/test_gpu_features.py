@@ -4,9 +4,9 @@ import pytest
 import torch
 
 from expert_grouped_gemm_gb300 import _lib
-from expert_grouped_gemm_gb300.inputs import custom, make_inputs
+from expert_grouped_gemm_gb300.inputs import WORKLOADS, custom, make_inputs
 from expert_grouped_gemm_gb300.layer import MoELayer
-from tests.parity import run_gpu
+from tests.parity import check_parity, planned_parity_case, run_gpu, run_oracle_replay
 
 pytestmark = pytest.mark.gpu
 
@@ -46,23 +46,36 @@ def test_recompute_mode_is_bitwise_equal(quota):
         assert np.array_equal(ref[n], rec[n]), n
 
 
-@pytest.mark.parametrize("rho", [(1, 2), (1, 4), (3, 2)])
-def test_device_quota_planner(rho):
+# [PR44] Compatibility and limits: keep_graph=False (nothing kept between the forward and
+# the backward) must give the same gradients; here the recompute mode is compared with the
+# fp64 oracle itself, not only with the saved mode.
+@pytest.mark.parametrize("name,kw", [
+    ("medium_bf16_retained", dict(T=300, H=256, F=192, E=16, k=4, zipf_s=1.0, F_shared=128, quota_factor=0.5)),
+    ("medium_bf16_full", dict(T=300, H=256, F=192, E=16, k=4, zipf_s=1.0, F_shared=128)),
+    ("qwen3_t4096_retained_s1.0", None),
+])
+def test_recompute_mode_matches_oracle(name, kw):
+    w = WORKLOADS[name] if kw is None else custom(name, **kw)
+    inp = make_inputs(w, seed=0)
+    layer = MoELayer(w, inp, record_routing=True, recompute=True)
+    g, _ = run_gpu(w, inp, layer=layer)
+    fwd, bwd = run_oracle_replay(w, inp, g)
+    rep = check_parity(w, g, fwd, bwd, inp)
+    print(name, "recompute", rep)
+
+
+# [LRMoE] Abstract: the forward plans retention quotas under resource constraints. The
+# device-planned quota, the selection it drives and the retained backward are compared
+# with the oracle, which plans its own quota from the same routing.
+@pytest.mark.parametrize("rho,budget", [((1, 2), None), ((1, 4), None), ((3, 2), None), ((1, 1), "mixed")])
+def test_device_quota_planner_matches_oracle(rho, budget):
     w = custom("planner", T=500, H=128, F=128, E=32, k=4, zipf_s=1.2)
-    inp = make_inputs(w, seed=8)
-    layer = MoELayer(w, inp, record_routing=True)
-    x, dy = inp["x"].cuda(), inp["dy"].cuda()
-    layer.forward(x)
-    quota = torch.empty(w.E, dtype=torch.int32, device="cuda")
-    _lib.moe_plan_quota(layer.dims, layer.ws, rho[0], rho[1], quota)
-    count = np.diff(layer.offsets.cpu().numpy().astype(np.int64))
-    cap = -(-rho[0] * w.T * w.k // (rho[1] * w.E))
-    assert quota.cpu().numpy().tolist() == np.minimum(count, cap).tolist()
-    budget = torch.tensor(np.arange(w.E) % 5 - 1, dtype=torch.int32, device="cuda")   # includes a negative
-    _lib.moe_plan_quota(layer.dims, layer.ws, rho[0], rho[1], quota, budget=budget)
-    expect = np.minimum(np.minimum(count, cap), np.maximum(budget.cpu().numpy(), 0))
-    assert quota.cpu().numpy().tolist() == expect.tolist()
-    layer.select(dy, quota)
-    assert int(layer.ret_offsets[-1].item()) == int(expect.sum())
-    layer.backward(dy, x, True)
-    assert _lib.moe_read_status(layer.ws) == _lib.MOE_OK
+    bud = (np.arange(w.E) % 5 - 1) * 9 if budget == "mixed" else None   # includes negatives and zeros
+    rep, g, _ = planned_parity_case(w, rho, bud, seed=8)
+    print(rho, budget, rep)
+
+
+def test_device_quota_planner_full_size():
+    rep, g, _ = planned_parity_case(WORKLOADS["qwen3_t4096_full"], (1, 2), seed=0)
+    assert rep["quota_sum"] == rep["R"]
+    print(rep)
