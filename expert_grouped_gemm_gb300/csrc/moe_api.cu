@@ -455,6 +455,13 @@ int expert_forward_gemms(const WsLayout& L, const WsPtrs& p, int bf, int sms, cu
 // Hooks for the other translation units of the library (not part of the C ABI).
 namespace moe {
 int internal_check_dims(const moe_dims* d) { return check_dims(d); }
+// The K split moe_fwd uses for the router logits GEMM at these dims on a GPU of `sms` SMs
+// (1: none). Valid dims only.
+int internal_router_ksplit(const moe_dims* d, int sms) {
+  if (d->dtype != MOE_BF16) return 1;
+  const WsLayout L = make_layout(d);
+  return ksplit_for(L, ((L.T + 127) / 128) * ((L.E + 127) / 128), (int)(L.H / kTileK), sms, L.T * L.E);
+}
 int internal_fail(int code, const char* msg) { return fail(code, "%s", msg); }
 void internal_count_launches(int n) { g_launches += n; }
 }  // namespace moe
@@ -587,7 +594,7 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
   CK(cudaMemsetAsync(p.status, 0, sizeof(int), st));
 
   // router logits = x W_r  (fp32 out; bias added by the top-k kernel)
-  const int rks = bf ? ksplit_for(L, ((L.T + 127) / 128) * ((L.E + 127) / 128), H / kTileK, sms, L.T * L.E) : 1;
+  const int rks = moe::internal_router_ksplit(dims, sms);
   {
     GemmArgs a = base_args(p.status);
     a.var_k = 0;

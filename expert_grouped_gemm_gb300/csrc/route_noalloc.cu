@@ -5,17 +5,25 @@
 // inside an allocator-less runtime (an inference engine whose memory pool is
 // fixed up front, a plugin that must not touch the caller's allocator, a
 // process that has to stay inside a pre-sized memory budget). For them this
-// entry point computes exactly what moe_fwd reports about routing -- top-k
-// experts and weights per token, per-expert offsets and the expert-contiguous
-// row of every pair -- with all of its scratch memory in one file-scope
-// device array of fixed size. Every GPU that loads the library keeps that
-// array until the process exits.
+// entry point computes what moe_fwd reports about routing -- top-k experts and
+// weights per token, per-expert offsets and the expert-contiguous row of every
+// pair -- with all of its scratch memory in one file-scope device array of
+// fixed size. Every GPU that loads the library keeps that array until the
+// process exits.
+//
+// The router GEMM runs with the K split moe_fwd picks for the same dims (its
+// fp32 partials live in the scratch, split 0 doubling as the logits buffer),
+// so the results are bit-identical to moe_fwd's whenever that split fits; a
+// smaller split is used otherwise, which changes only the fp32 summation
+// order of the logits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
-#include <unordered_map>
+#include <utility>
 
 #include "common.cuh"
 #include "gemm_launch.h"
@@ -25,16 +33,20 @@ namespace moe {
 int internal_check_dims(const moe_dims* d);
 int internal_fail(int code, const char* msg);
 void internal_count_launches(int n);
+int internal_router_ksplit(const moe_dims* d, int sms);
 }  // namespace moe
 
 using namespace moe;
 
 namespace {
 
-// Largest scratch the routing stage may use: biased fp32 logits [T,E], the
-// per-chunk expert masks and row bases, the per-expert counters and the
-// padded pair/row maps. T*E <= 1,048,576 with k <= 8 fits (e.g. T=8192, E=128).
-constexpr size_t kRouteScratchBytes = size_t(8) << 20;
+// Size of the fixed scratch. What the routing stage keeps there, in bytes (each
+// entry rounded up to 256): a status word; the router logits, 4*ks*T*E (ks = the
+// router GEMM's K split, 1 without one); the per-64-token expert masks and row bases,
+// 12*ceil(T/64)*E; per-expert counts and offsets, about 16*E; the padded row of
+// every pair, 4*T*k; the pair of every padded row, 4*(T*k + 15*E). With ks = 1 the
+// total is about 4*T*E + 12*ceil(T/64)*E + 8*T*k + 76*E bytes.
+constexpr size_t kRouteScratchBytes = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_route_scratch[kRouteScratchBytes];
 
@@ -44,12 +56,12 @@ struct ScratchLayout {
   size_t status, logits, masks, chunk_base, count, offset, pad_off, tile_off, rowp, pair_of_row, total;
 };
 
-ScratchLayout scratch_layout(const moe_dims* d) {
+ScratchLayout scratch_layout(const moe_dims* d, int ks) {
   const size_t T = d->T, E = d->E, k = d->k, P = T * k, C = (T + 63) / 64, R = P + 15 * E;
   ScratchLayout L;
   size_t o = 0;
   L.status = o;      o += up256(sizeof(int));
-  L.logits = o;      o += up256(T * E * sizeof(float));
+  L.logits = o;      o += up256((size_t)ks * T * E * sizeof(float));
   L.masks = o;       o += up256(C * E * sizeof(uint64_t));
   L.chunk_base = o;  o += up256(C * E * sizeof(int));
   L.count = o;       o += up256(E * sizeof(int));
@@ -62,20 +74,42 @@ ScratchLayout scratch_layout(const moe_dims* d) {
   return L;
 }
 
-// Device address of the scratch array on the current device, looked up once
-// per device. The host-side name g_route_scratch is only a stand-in for the
+// Device address of the scratch array in the current CUDA context. The lookup is
+// done once per (device, context) and kept: a context that was torn down and made
+// again (after cudaDeviceReset, for example) gets a fresh lookup, so a stale address
+// is never used. The host-side name g_route_scratch is only a stand-in for the
 // device symbol and must never be handed to a kernel.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
 int scratch_address(unsigned char** out) {
   static std::mutex mu;
-  static std::unordered_map<int, unsigned char*> addr;
+  static std::map<std::pair<int, uintptr_t>, unsigned char*> addr;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return internal_fail(MOE_ERR_CUDA, "cudaGetDevice failed");
+  CtxGetCurrentFn get_ctx = ctx_get_current();
+  CUcontext ctx = nullptr;
+  if (get_ctx) get_ctx(&ctx);
   std::lock_guard<std::mutex> lk(mu);
-  auto it = addr.find(dev);
-  if (it != addr.end()) {
-    *out = it->second;
-    return MOE_OK;
+  if (ctx) {
+    auto it = addr.find({dev, reinterpret_cast<uintptr_t>(ctx)});
+    if (it != addr.end()) {
+      *out = it->second;
+      return MOE_OK;
+    }
   }
   void* p = nullptr;
   e = cudaGetSymbolAddress(&p, g_route_scratch);
@@ -84,7 +118,9 @@ int scratch_address(unsigned char** out) {
     snprintf(msg, sizeof(msg), "cudaGetSymbolAddress(route scratch) failed: %s", cudaGetErrorString(e));
     return internal_fail(MOE_ERR_CUDA, msg);
   }
-  addr[dev] = static_cast<unsigned char*>(p);
+  // the lookup made the runtime's context current if it was not yet
+  if (get_ctx && (ctx != nullptr || get_ctx(&ctx) == CUDA_SUCCESS) && ctx)
+    addr[{dev, reinterpret_cast<uintptr_t>(ctx)}] = static_cast<unsigned char*>(p);
   *out = static_cast<unsigned char*>(p);
   return MOE_OK;
 }
@@ -110,23 +146,34 @@ extern "C" MOE_API int moe_route_noalloc(const moe_dims* dims, void* stream, con
   if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(router_bias, 4) || !aligned(topk_idx, 4) ||
       !aligned(topk_w, 4) || !aligned(expert_offsets, 4) || !aligned(row_of_pair, 4) || !aligned(device_status, 4))
     return internal_fail(MOE_ERR_INVALID_ARG, "moe_route_noalloc: misaligned pointer");
-  const ScratchLayout L = scratch_layout(dims);
-  if (L.total > kRouteScratchBytes) {
-    char msg[200];
+  const ScratchLayout L1 = scratch_layout(dims, 1);
+  if (L1.total > kRouteScratchBytes) {
+    char msg[240];
     snprintf(msg, sizeof(msg),
              "moe_route_noalloc: these dims need %zu bytes of routing scratch, more than the fixed %zu bytes "
-             "(keep T*E <= 1048576 with k <= 8, or use moe_fwd with a workspace)",
-             L.total, kRouteScratchBytes);
+             "(about 4*T*E + 12*ceil(T/64)*E + 8*T*k + 76*E bytes must fit; use moe_fwd with a workspace)",
+             L1.total, kRouteScratchBytes);
     return internal_fail(MOE_ERR_UNSUPPORTED, msg);
   }
   unsigned char* base = nullptr;
   if ((rc = scratch_address(&base))) return rc;
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int sms = sms_of_current_device();
   const int T = (int)dims->T, H = (int)dims->H, E = (int)dims->E, k = (int)dims->k;
   const int C = (T + 63) / 64;
+  // moe_fwd's K split of the router GEMM; fewer splits if their partials do not fit
+  int ks = internal_router_ksplit(dims, sms);
+  while (ks > 1 && scratch_layout(dims, ks).total > kRouteScratchBytes) --ks;
+  if (ks > 1) {  // the same normalisation moe_fwd applies: no split without k-blocks
+    const int kblocks = H / 64;
+    const int per = (kblocks + ks - 1) / ks;
+    ks = (kblocks + per - 1) / per;
+  }
+  const ScratchLayout L = scratch_layout(dims, ks);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* status = device_status ? device_status : reinterpret_cast<int*>(base + L.status);
-  float* logits = reinterpret_cast<float*>(base + L.logits);
+  float* logits = reinterpret_cast<float*>(base + L.logits);  // split s at logits + s*T*E
   uint64_t* masks = reinterpret_cast<uint64_t*>(base + L.masks);
   int* chunk_base = reinterpret_cast<int*>(base + L.chunk_base);
   int* count = reinterpret_cast<int*>(base + L.count);
@@ -141,8 +188,10 @@ extern "C" MOE_API int moe_route_noalloc(const moe_dims* dims, void* stream, con
     snprintf(msg, sizeof(msg), "moe_route_noalloc: %s: %s", what, cudaGetErrorString(e));
     return internal_fail(MOE_ERR_CUDA, msg);
   };
-  // Only the status word must start at zero: every other scratch entry is
-  // fully written by the kernel that produces it before anything reads it.
+  // Only the status word must start at zero (the expert masks are cleared by the
+  // top-k launcher): every other scratch entry is fully written by the kernel that
+  // produces it before anything reads it, so what an earlier call left there is
+  // never read.
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
 
@@ -163,9 +212,16 @@ extern "C" MOE_API int moe_route_noalloc(const moe_dims* dims, void* stream, con
   a.epi = EPI_F32;
   a.out0 = logits;
   a.ldo = E;
-  e = dims->dtype == MOE_BF16 ? launch_tc_gemm(a, 128, st, sms_of_current_device(), 0) : launch_simt_gemm_f32(a, st);
+  if (ks > 1) {  // every split writes its fp32 partial sums; the top-k kernel adds them in split order
+    a.ksplit = ks;
+    a.part_stride = (int64_t)T * E;
+  }
+  e = dims->dtype == MOE_BF16 ? launch_tc_gemm(a, 128, st, sms, 0) : launch_simt_gemm_f32(a, st);
   if (e != cudaSuccess) return cuda_fail(e, "router GEMM");
-  if ((e = launch_route_topk(logits, router_bias, T, E, k, topk_idx, topk_w, masks, st)) != cudaSuccess)
+  // with a split, the top-k kernel reads every split of a token's row before it writes
+  // the biased logits over split 0 of that row (same thread, same elements)
+  if ((e = launch_route_topk(logits, router_bias, T, E, k, topk_idx, topk_w, masks, st, ks > 1 ? logits : nullptr, ks,
+                             (int64_t)T * E)) != cudaSuccess)
     return cuda_fail(e, "top-k");
   if ((e = launch_route_scan(masks, C, E, count, offset, pad_off, tile_off, chunk_base, pair_of_row, expert_offsets,
                              st)) != cudaSuccess)

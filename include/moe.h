@@ -176,25 +176,35 @@ MOE_API int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* strea
  * is fixed up front, a plugin that must not touch its host's allocator, a
  * process held to a pre-sized memory budget. The pages this library follows
  * have no counterpart to it; it exists only for those callers.
- *   Computes the same values moe_fwd reports through its optional outputs:
+ *   Computes the routing moe_fwd reports through its optional outputs:
  *   router logits x w_router + router_bias (fp32), top-k experts per token
  *   (ties to the lower index), softmax-renormalised weights, per-expert
- *   exclusive offsets and the expert-contiguous row of every pair.
+ *   exclusive offsets and the expert-contiguous row of every pair. The router
+ *   GEMM runs with the same K split as moe_fwd whenever its fp32 partial sums
+ *   fit in the scratch, and the results are then bit-identical to moe_fwd's;
+ *   otherwise it runs with fewer splits, the logits are summed in another
+ *   order, and an index may differ from moe_fwd's at a near tie.
  * Inputs:  x[T,H], w_router[H,E] (dims.dtype), router_bias[E] float (nullable).
  * Outputs (all required, device): topk_idx[T,k] int32, topk_w[T,k] float,
  *          expert_offsets[E+1] int32, row_of_pair[T*k] int32;
  *          device_status (nullable, one int32 on the device): set to MOE_OK,
  *          or to MOE_ERR_TIMEOUT if a bounded wait inside a kernel ran out.
- * Scratch: one fixed array of 8 MiB in the library's device memory (every
+ * Scratch: one fixed array of 32 MiB in the library's device memory (every
  *          GPU that loads the library holds it until the process exits).
- *          Dims whose scratch would not fit (roughly T*E > 1,048,576 at
- *          k <= 8) are rejected with MOE_ERR_UNSUPPORTED before any work.
+ *          Without a K split the call needs about
+ *          4*T*E + 12*ceil(T/64)*E + 8*T*k + 76*E bytes of it (each of ten
+ *          entries rounded up to 256 bytes); a K split of ks parts adds
+ *          4*(ks-1)*T*E. Dims that do not fit without a split are rejected with
+ *          MOE_ERR_UNSUPPORTED before any work (T=8192, E=128, k=8 needs 9.1 MB
+ *          with its split of 2; at k = 8 the largest T that fits is about
+ *          55,800 for E=128, 256,000 for E=16 and 7,600 for E=1024).
  *          Every call on a device uses the same array and leaves its
- *          contents behind: calls that overlap on the GPU (two streams, or
- *          two threads without ordering) race on it and must be serialised.
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
- * Calls no cudaMalloc/cudaFree or allocating library routine.
+ *          contents behind (nothing an earlier call left is ever read): calls
+ *          that overlap on the GPU (two streams, or two threads without
+ *          ordering) race on it and must be serialised.
+ * The first call in each CUDA context looks up the array's device address
+ * (cudaGetSymbolAddress) and keeps it; make that first call before any stream
+ * capture. Calls no cudaMalloc/cudaFree or allocating library routine.
  */
 MOE_API int moe_route_noalloc(const moe_dims* dims, void* stream, const void* x, const void* w_router,
                               const float* router_bias, int32_t* topk_idx, float* topk_w,
