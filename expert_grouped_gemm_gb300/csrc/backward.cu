@@ -86,77 +86,104 @@ __global__ void __launch_bounds__(256) k_pair_score(const TIO* dy, const TIO* y_
 }
 
 // ------------------------------------------------------------------ quota select
-__device__ __forceinline__ uint64_t sel_key(float s, int local) {
-  uint32_t u = __float_as_uint(s);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // order-preserving
-  return ((uint64_t)u << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)local);
+// Order-preserving map of an fp32 score to an unsigned key (larger score, larger key).
+__device__ __forceinline__ uint32_t score_key(float s) {
+  const uint32_t u = __float_as_uint(s);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block per expert (256 threads). Finds the q-th largest (score, -token) key by
-// an 8-pass MSB-first radix select over 8-bit digits, keeps keys >= it, and
-// numbers the kept rows in row order.
-__global__ void __launch_bounds__(256) k_select(const float* score, const int* count, const int* pad_off,
-                                                const int* quota, int* ret_cidx, int* ret_count, int* status) {
+constexpr int kSelThreads = 512;
+constexpr int kSelCache = 8192;  // keys of an expert kept in shared memory (rows past it are re-read)
+
+// Block per expert. The kept rows are the q largest by (score descending, token
+// ascending); rows of an expert are in token order, so among rows of equal score the
+// earlier rows win. Steps: (1) a 4-pass MSB-first radix select over the 32-bit score
+// keys finds the key of the q-th largest row and how many rows of exactly that key are
+// still needed; each pass builds a 256-bin histogram of the rows that match the
+// prefix found so far, and a suffix scan over the bins (in parallel) picks the bin the
+// q-th row falls in; (2) one pass over the rows in row order keeps every row with a
+// larger key and the first `need` rows with an equal key, and numbers the kept rows.
+__global__ void __launch_bounds__(kSelThreads) k_select(const float* score, const int* count, const int* pad_off,
+                                                        const int* quota, int* ret_cidx, int* ret_count,
+                                                        int* status) {
+  __shared__ uint32_t s_key[kSelCache];
   __shared__ int hist[256];
-  __shared__ uint64_t s_prefix, s_mask;
+  __shared__ int wtot[kSelThreads / 32];
+  __shared__ uint32_t s_prefix;
   __shared__ int s_need;
-  __shared__ int s_carry;
   const int e = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cnt = count[e];
   const int base = pad_off[e];
   int q = cnt;
   if (quota) {
     const int qq = quota[e];
-    if (qq < 0 && threadIdx.x == 0) set_status(status, MOE_ERR_DEVICE_ARG);
+    if (qq < 0 && tid == 0) set_status(status, MOE_ERR_DEVICE_ARG);
     q = min(max(qq, 0), cnt);
   }
-  uint64_t thr = 0;  // keep keys >= thr
-  bool keep_all = (q == cnt), keep_none = (q == 0);
+  const bool keep_all = (q == cnt), keep_none = (q == 0);
+  const int cached = min(cnt, kSelCache);
+  auto key_of = [&](int i) -> uint32_t { return i < kSelCache ? s_key[i] : score_key(score[base + i]); };
+  uint32_t thr = 0;
+  int need_eq = 0;
   if (!keep_all && !keep_none) {
-    if (threadIdx.x == 0) {
+    for (int i = tid; i < cached; i += kSelThreads) s_key[i] = score_key(score[base + i]);
+    if (tid == 0) {
       s_prefix = 0;
-      s_mask = 0;
       s_need = q;
     }
-    __syncthreads();
-    for (int d = 56; d >= 0; d -= 8) {
-      hist[threadIdx.x] = 0;
+    uint32_t mask = 0;
+    for (int d = 24; d >= 0; d -= 8) {
+      if (tid < 256) hist[tid] = 0;
       __syncthreads();
-      const uint64_t pre = s_prefix, msk = s_mask;
-      for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
-        const uint64_t key = sel_key(score[base + i], i);
-        if ((key & msk) == pre) atomicAdd(&hist[(key >> d) & 0xFF], 1);
+      const uint32_t pre = s_prefix;
+      for (int i = tid; i < cnt; i += kSelThreads) {
+        const uint32_t kk = key_of(i);
+        if ((kk & mask) == pre) atomicAdd(&hist[(kk >> d) & 0xFFu], 1);
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        int need = s_need, acc = 0, b = 255;
-        for (; b > 0; --b) {
-          if (acc + hist[b] >= need) break;
-          acc += hist[b];
+      // suffix sums over the bins from the top: thread j holds bin 255 - j
+      const int need = s_need;
+      int v = tid < 256 ? hist[255 - tid] : 0, incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31 && warp < 8) wtot[warp] = incl;
+      __syncthreads();
+      if (tid < 256) {
+        for (int w2 = 0; w2 < warp; ++w2) incl += wtot[w2];
+        const int excl = incl - v;
+        if (excl < need && incl >= need) {  // exactly one bin holds the q-th largest row
+          s_prefix = pre | ((uint32_t)(255 - tid) << d);
+          s_need = need - excl;
         }
-        s_need = need - acc;
-        s_prefix = pre | ((uint64_t)b << d);
-        s_mask = msk | (0xFFull << d);
       }
+      mask |= 0xFFu << d;
       __syncthreads();
     }
     thr = s_prefix;
+    need_eq = s_need;
   }
-  // number kept rows in row order
-  if (threadIdx.x == 0) s_carry = 0;
-  __syncthreads();
-  for (int i0 = 0; i0 < cnt; i0 += blockDim.x) {
-    const int i = i0 + threadIdx.x;
-    bool kept = false;
-    if (i < cnt) kept = keep_all || (!keep_none && sel_key(score[base + i], i) >= thr);
-    int tot;
-    const int pos = block_excl_scan(kept ? 1 : 0, &tot);
-    if (i < cnt) ret_cidx[base + i] = kept ? s_carry + pos : -1;
-    __syncthreads();
-    if (threadIdx.x == 0) s_carry += tot;
-    __syncthreads();
+  // number the kept rows in row order; rows with key == thr are kept while their rank
+  // among the equal rows (in row order, i.e. token order) is below need_eq
+  int carry_kept = 0, carry_eq = 0;
+  for (int i0 = 0; i0 < cnt; i0 += kSelThreads) {
+    const int i = i0 + tid;
+    uint32_t kk = 0;
+    if (i < cnt && !keep_all && !keep_none) kk = key_of(i);
+    const int eq = (i < cnt && !keep_all && !keep_none && kk == thr) ? 1 : 0;
+    int eq_tot;
+    const int eq_rank = carry_eq + block_excl_scan(eq, &eq_tot);
+    const bool kept = i < cnt && (keep_all || (!keep_none && (kk > thr || (eq && eq_rank < need_eq))));
+    int kept_tot;
+    const int pos = carry_kept + block_excl_scan(kept ? 1 : 0, &kept_tot);
+    if (i < cnt) ret_cidx[base + i] = kept ? pos : -1;
+    carry_kept += kept_tot;
+    carry_eq += eq_tot;
   }
-  if (threadIdx.x == 0) ret_count[e] = q;
+  if (tid == 0) ret_count[e] = q;
 }
 
 // One block of 1024 threads: offsets of the kept rows, exact and padded.
@@ -214,15 +241,9 @@ __global__ void k_ret_index(const int* topk_idx, const int* rowp_of_pair, const 
   }
 }
 
-// Warp per compact row: copy x_t, a|b, h of the kept pair and write w dY_t.
-template <typename TIO>
-__device__ __forceinline__ void copy_row(TIO* dst, const TIO* src, int n, int lane) {
-  if constexpr (sizeof(TIO) == 2) {
-    for (int i = lane; i < n / 8; i += 32) reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
-  } else {
-    for (int i = lane; i < n; i += 32) dst[i] = src[i];
-  }
-}
+// Warp per compact row: copy x_t, a|b, h of the kept pair and write w dY_t. The four
+// row segments go through one copy loop (so one set of registers serves them all); bf16
+// rows move as 16-byte vectors with eight loads in flight per lane before their stores.
 template <typename TIO>
 __device__ __forceinline__ void zero_row(TIO* dst, int n, int lane) {
   if constexpr (sizeof(TIO) == 2) {
@@ -255,20 +276,42 @@ __global__ void __launch_bounds__(256) k_compact_rows(const int* ret_src, const 
     const int p = pair_of_row[src];
     const int t = p / k;
     const float w = topk_w[p];
-    copy_row(xd, x + (int64_t)t * H, H, lane);
-    copy_row(abd, ab + (int64_t)src * 2 * F, 2 * F, lane);
-    copy_row(hd, h + (int64_t)src * F, F, lane);
-    const TIO* dyr = dy + (int64_t)t * H;
-    if constexpr (sizeof(TIO) == 2) {
-      for (int i = lane; i < H / 8; i += 32) {
-        float a[8];
-        bf16x8_to_f(reinterpret_cast<const uint4*>(dyr)[i], a);
+#pragma unroll 1
+    for (int seg = 0; seg < 4; ++seg) {
+      const TIO* sp = seg == 0 ? x + (int64_t)t * H
+                    : seg == 1 ? ab + (int64_t)src * 2 * F
+                    : seg == 2 ? h + (int64_t)src * F
+                               : dy + (int64_t)t * H;
+      TIO* dp = seg == 0 ? xd : seg == 1 ? abd : seg == 2 ? hd : dyd;
+      const int n = (seg == 0 || seg == 3) ? H : seg == 1 ? 2 * F : F;
+      const bool scaled = seg == 3;  // w * dY_t, rounded once
+      if constexpr (sizeof(TIO) == 2) {
+        const int nv = n / 8;
+        const uint4* s4 = reinterpret_cast<const uint4*>(sp);
+        uint4* d4 = reinterpret_cast<uint4*>(dp);
+#pragma unroll 1
+        for (int i0 = lane; i0 < nv; i0 += 32 * 8) {
+          uint4 u[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) a[q] *= w;
-        reinterpret_cast<uint4*>(dyd)[i] = f_to_bf16x8(a);
+          for (int j = 0; j < 8; ++j)
+            if (i0 + 32 * j < nv) u[j] = s4[i0 + 32 * j];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (i0 + 32 * j < nv) {
+              if (scaled) {
+                float a[8];
+                bf16x8_to_f(u[j], a);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) a[q] *= w;
+                u[j] = f_to_bf16x8(a);
+              }
+              d4[i0 + 32 * j] = u[j];
+            }
+          }
+        }
+      } else {
+        for (int i = lane; i < n; i += 32) dp[i] = scaled ? io<TIO>::cvt(w * io<TIO>::to_f(sp[i])) : sp[i];
       }
-    } else {
-      for (int i = lane; i < H; i += 32) dyd[i] = io<TIO>::cvt(w * io<TIO>::to_f(dyr[i]));
     }
   }
 }
@@ -429,7 +472,7 @@ cudaError_t launch_pair_score(const void* dy, const void* y_pair, const int* pai
 
 cudaError_t launch_select(const float* score, const int* count, const int* pad_off, const int* quota, int E,
                           int* ret_cidx, int* ret_count, int* status, cudaStream_t st) {
-  k_select<<<E, 256, 0, st>>>(score, count, pad_off, quota, ret_cidx, ret_count, status);
+  k_select<<<E, kSelThreads, 0, st>>>(score, count, pad_off, quota, ret_cidx, ret_count, status);
   return cudaGetLastError();
 }
 
@@ -479,47 +522,47 @@ cudaError_t launch_transpose(const void* in, int R, int Cc, void* out, cudaStrea
   return cudaGetLastError();
 }
 
-// bf16, k <= 8: persistent blocks; the next token's slot metadata is loaded by k
-// threads while this token's rows are in flight and handed over through shared
-// memory at the token boundary. Same summation order as k_dx_reduce.
-__global__ void __launch_bounds__(256, 2) k_dx_reduce_k8(const __nv_bfloat16* __restrict__ dx_pair,
+// bf16, k <= 8: warp per token, grid-stride. Lane j < k loads slot j's compact row,
+// expert and router-logit gradient and shuffles hand them to the other lanes, so a warp
+// needs no block barrier and many tokens are in flight per SM. Each lane owns 8
+// consecutive columns per 256-column step and issues every slot's dx_pair and
+// router-weight row loads of the step before it sums them. Same summation order as
+// k_dx_reduce (kept slots ascending, then the router term slot by slot, then shared).
+__global__ void __launch_bounds__(256) k_dx_reduce_k8(const __nv_bfloat16* __restrict__ dx_pair,
                                                       const int* __restrict__ crow_of_pair,
                                                       const int* __restrict__ topk_idx, const float* __restrict__ dl_sel,
                                                       const __nv_bfloat16* __restrict__ wrT,
                                                       const __nv_bfloat16* __restrict__ sh_dx, int T, int H, int k,
                                                       __nv_bfloat16* __restrict__ dx) {
-  __shared__ int s_c[2][8], s_e[2][8];
-  __shared__ float s_d[2][8];
-  const int tid = threadIdx.x;
-  int t = blockIdx.x, buf = 0;
-  if (tid < 8) {
-    const bool v = tid < k && t < T;
-    s_c[0][tid] = v ? crow_of_pair[(int64_t)t * k + tid] : -1;
-    s_e[0][tid] = v ? topk_idx[(int64_t)t * k + tid] : 0;
-    s_d[0][tid] = v ? dl_sel[(int64_t)t * k + tid] : 0.0f;
-  }
-  __syncthreads();
-  for (; t < T; t += gridDim.x) {
-    const int tn = t + gridDim.x;
-    int c_next = -1, e_next = 0;
-    float d_next = 0.0f;
-    if (tid < k && tn < T) {
-      c_next = crow_of_pair[(int64_t)tn * k + tid];
-      e_next = topk_idx[(int64_t)tn * k + tid];
-      d_next = dl_sel[(int64_t)tn * k + tid];
+  const int lane = threadIdx.x & 31;
+  const int nv = H / 8;
+  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
+    int c = -1, ex = 0;
+    float d = 0.0f;
+    if (lane < k) {
+      c = crow_of_pair[(int64_t)t * k + lane];
+      ex = topk_idx[(int64_t)t * k + lane];
+      d = dl_sel[(int64_t)t * k + lane];
     }
-    for (int i = tid; i < H / 8; i += blockDim.x) {
-      uint4 u[8], v[8];  // the slots' dx_pair rows and router-weight rows, all loads in flight together
+    int cj[8], ej[8];
+    float dj[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // lanes j >= k hold c = -1, d = 0
+      cj[j] = __shfl_sync(0xffffffffu, c, j);
+      ej[j] = __shfl_sync(0xffffffffu, ex, j);
+      dj[j] = __shfl_sync(0xffffffffu, d, j);
+    }
+    for (int i = lane; i < nv; i += 32) {
+      uint4 u[8], v[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int cr = s_c[buf][j];
-        u[j] = cr >= 0 ? reinterpret_cast<const uint4*>(dx_pair + (int64_t)cr * H)[i] : make_uint4(0, 0, 0, 0);
-        if (j < k) v[j] = reinterpret_cast<const uint4*>(wrT + (int64_t)s_e[buf][j] * H)[i];
+        u[j] = cj[j] >= 0 ? reinterpret_cast<const uint4*>(dx_pair + (int64_t)cj[j] * H)[i] : make_uint4(0, 0, 0, 0);
+        v[j] = j < k ? reinterpret_cast<const uint4*>(wrT + (int64_t)ej[j] * H)[i] : make_uint4(0, 0, 0, 0);
       }
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, f[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        if (s_c[buf][j] >= 0) {
+        if (cj[j] >= 0) {
           bf16x8_to_f(u[j], f);
 #pragma unroll
           for (int q = 0; q < 8; ++q) acc[q] += f[q];
@@ -529,9 +572,8 @@ __global__ void __launch_bounds__(256, 2) k_dx_reduce_k8(const __nv_bfloat16* __
       for (int j = 0; j < 8; ++j) {
         if (j < k) {
           bf16x8_to_f(v[j], f);
-          const float d = s_d[buf][j];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] = fmaf(d, f[q], acc[q]);
+          for (int q = 0; q < 8; ++q) acc[q] = fmaf(dj[j], f[q], acc[q]);
         }
       }
       if (sh_dx) {
@@ -541,13 +583,6 @@ __global__ void __launch_bounds__(256, 2) k_dx_reduce_k8(const __nv_bfloat16* __
       }
       reinterpret_cast<uint4*>(dx + (int64_t)t * H)[i] = f_to_bf16x8(acc);
     }
-    if (tid < 8) {
-      s_c[buf ^ 1][tid] = c_next;
-      s_e[buf ^ 1][tid] = e_next;
-      s_d[buf ^ 1][tid] = d_next;
-    }
-    __syncthreads();
-    buf ^= 1;
   }
 }
 
@@ -556,10 +591,10 @@ cudaError_t launch_dx_reduce(const void* dx_pair, const int* crow_of_pair, const
                              const void* wrT, const void* sh_dx, int T, int H, int k, void* dx, int num_sms,
                              cudaStream_t st) {
   if (sizeof(TIO) == 2 && k <= 8) {
-    int per_sm = 0;  // persistent: as many blocks as fit at once
+    int per_sm = 0;  // grid-stride over tokens with as many blocks as fit at once
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_dx_reduce_k8, 256, 0) != cudaSuccess || per_sm < 1)
       per_sm = 1;
-    const int g = (int)std::max<int64_t>(1, std::min<int64_t>(T, (int64_t)num_sms * per_sm));
+    const int g = (int)std::max<int64_t>(1, std::min<int64_t>(((int64_t)T + 7) / 8, (int64_t)num_sms * per_sm));
     k_dx_reduce_k8<<<g, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(dx_pair), crow_of_pair, topk_idx, dl_sel,
                                       reinterpret_cast<const __nv_bfloat16*>(wrT),
                                       reinterpret_cast<const __nv_bfloat16*>(sh_dx), T, H, k,

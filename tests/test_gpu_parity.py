@@ -153,3 +153,21 @@ def test_parity_full_size_glm(name):
     cnt = np.diff(g["offsets"])
     assert np.sum(cnt == 0) >= 1, "expected some zero-token experts"
     print(name, rep)
+
+
+# --------------------------------------------------------------- selection with score ties
+@pytest.mark.parametrize("distinct", [1, 5])
+def test_selection_with_massive_score_ties(distinct):
+    """Tokens copied from `distinct` different rows (x and dY alike), so the pair scores
+    w * ||dY_t|| * ||x_t|| of an expert take at most `distinct` values and the quota
+    boundary falls inside a run of equal scores: the kept rows must be the lowest tokens
+    of that run, exactly as the oracle ranks them (score descending, token ascending)."""
+    w = custom(f"ties{distinct}", T=384, H=128, F=128, E=16, k=2, zipf_s=0.5, quota_factor=0.3)
+    inp = make_inputs(w, seed=9)
+    g = torch.Generator().manual_seed(distinct)
+    src = torch.randint(0, distinct, (w.T,), generator=g)
+    inp["x"] = inp["x"][src].contiguous()
+    inp["dy"] = inp["dy"][src].contiguous()
+    rep, res, *_ = parity_case(w, inp=inp)
+    assert rep["R"] == int(np.minimum(np.diff(res["offsets"]), w.quota_per_expert()).sum())
+    print(distinct, rep)
