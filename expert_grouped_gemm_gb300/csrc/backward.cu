@@ -189,7 +189,8 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const float* score, cons
 // One block of 1024 threads: offsets of the kept rows, exact and padded.
 __global__ void __launch_bounds__(1024) k_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off,
                                                    int* ret_tile_off, int* ret_src, int* user_offsets, int* order,
-                                                   int* ret_tile_off2, int4* tile_rec, int4* ord_rec) {
+                                                   int* ret_tile_off2, int4* tile_rec, int4* ord_rec,
+                                                   int4* tile_rec2) {
   const int e = threadIdx.x;
   const int cnt = e < E ? ret_count[e] : 0;
   const int rank = order ? block_order_desc(cnt, E, order) : 0;
@@ -211,6 +212,8 @@ __global__ void __launch_bounds__(1024) k_ret_scan(const int* ret_count, int E, 
     for (int r = op + cnt; r < op + pad; ++r) ret_src[r] = -1;
     if (tile_rec)
       for (int j = 0; j < tiles; ++j) tile_rec[ot + j] = make_int4(e, j * 128, cnt, op);
+    if (tile_rec2)
+      for (int j = 0; j < tiles2; ++j) tile_rec2[ot2 + j] = make_int4(e, j * 256, cnt, op);
     if (ord_rec && order) ord_rec[rank] = make_int4(e, cnt, op, 0);
   }
   if (e == 0) {
@@ -478,9 +481,9 @@ cudaError_t launch_select(const float* score, const int* count, const int* pad_o
 
 cudaError_t launch_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off, int* ret_tile_off,
                             int* ret_src, int* user_offsets, cudaStream_t st, int* order, int* ret_tile_off2,
-                            int4* tile_rec, int4* ord_rec) {
+                            int4* tile_rec, int4* ord_rec, int4* tile_rec2) {
   k_ret_scan<<<1, 1024, 0, st>>>(ret_count, E, ret_offset, ret_pad_off, ret_tile_off, ret_src, user_offsets, order,
-                                 ret_tile_off2, tile_rec, ord_rec);
+                                 ret_tile_off2, tile_rec, ord_rec, tile_rec2);
   return cudaGetLastError();
 }
 

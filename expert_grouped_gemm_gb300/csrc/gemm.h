@@ -69,6 +69,7 @@ struct GemmArgs {
   // one per scheduled group {group, rows, row offset, 0}. Null: derive from the above.
   const int4* tile_rec;
   const int4* grp_rec;
+  const int4* tile_rec2;  // var-M, CTA-pair tiles: one record per 256-row block, same fields as tile_rec
   // K split (tensor cores, EPI_F32 only): every tile's k-blocks are divided over ksplit
   // CTAs (0 or 1: none); a split without k-blocks writes zeros
   int ksplit;

@@ -33,9 +33,13 @@ namespace moe {
 constexpr int kStageRowBytes = 128;                   // 64 bf16 per staged row
 constexpr int kStageTileBytes = 32 * kStageRowBytes;  // one warp's 32 rows x 64 columns (4 KB)
 
-// CTAs per 256-column tile for the expert GEMMs (1: one CTA; 2: CTA pair, M = 256).
-#ifndef MOE_GEMM_CTAS
-#define MOE_GEMM_CTAS 1
+// CTAs per tile of the variable-M expert GEMMs (gate/up, down, dH, dX): 1 = one CTA per
+// 128-row tile (default); 2 = CTA pair (cta_group::2, 256 rows by 256 columns; each CTA
+// loads its 128 rows of A and half of B, so a k-block costs a CTA 32 KB instead of 48 KB
+// and six stages fit in shared memory, but experts are padded to 256-row tiles). Pairs
+// measured slower at the Qwen3 and GLM-4.5 shapes. The variable-K dW GEMMs use one CTA.
+#ifndef MOE_VARM_CTAS
+#define MOE_VARM_CTAS 1
 #endif
 
 template <int BN, int STAGES, int EPI_WARP_BYTES, int CTAS, int NEPI>
@@ -74,6 +78,8 @@ __device__ __forceinline__ int4 load_tile_rec(const GemmArgs& a, int t, int NT) 
     if (a.grp_rec) return __ldg(a.grp_rec + t / (((a.M + TILE_M - 1) / TILE_M) * NT));
   } else if (TILE_M == kTileM && a.tile_rec) {
     return __ldg(a.tile_rec + t / NT);
+  } else if (TILE_M == 2 * kTileM && a.tile_rec2) {
+    return __ldg(a.tile_rec2 + t / NT);
   }
   return make_int4(0, 0, 0, 0);
 }
@@ -101,7 +107,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int NT
       ti.off = grp_off(a, ti.g);
     }
     ti.kblocks = (ti.rows + kTileK - 1) / kTileK;
-  } else if (TILE_M == kTileM && a.tile_rec) {
+  } else if ((TILE_M == kTileM && a.tile_rec) || (TILE_M == 2 * kTileM && a.tile_rec2)) {
     ti.nt = t - (t / NT) * NT;
     ti.g = rec.x;
     ti.m0 = rec.y;
@@ -733,7 +739,6 @@ static int staging_bytes(const GemmArgs& a) {
   if (a.epi == EPI_F32) return 0;
   if (a.epi == EPI_SWIGLU_FWD) return 2 * kStageTileBytes;
   if (a.epi == EPI_SWIGLU_BWD) return 2 * kStageTileBytes;  // a|b tiles, da|db staged in place
-  if (a.epi == EPI_DW && a.paired && MOE_GEMM_CTAS == 2) return 2 * kStageTileBytes;  // pair build: both staged
   return kStageTileBytes;
 }
 
@@ -746,9 +751,9 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_s
     if (a.epi == EPI_DW) return launch_cfg<128, 6, kT, EPI_DW, 1>(a, st, num_sms);
     return cudaErrorInvalidValue;
   }
-  // 256-column tiles (the CTA-pair variant, CTAS = 2, is kept but measured slower)
-#if MOE_GEMM_CTAS == 2
+  // 256-column tiles: the variable-M GEMMs as CTA pairs (or single CTAs), dW single CTAs
   switch (a.epi) {
+#if MOE_VARM_CTAS == 2
     case EPI_SWIGLU_BWD:
       if (need > 4 * kT) return cudaErrorInvalidValue;
       return launch_cfg<256, 5, 4 * kT, EPI_SWIGLU_BWD, 2>(a, st, num_sms);
@@ -758,16 +763,7 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_s
     case EPI_STORE:
       if (need > 2 * kT) return cudaErrorInvalidValue;
       return launch_cfg<256, 6, 2 * kT, EPI_STORE, 2>(a, st, num_sms);
-    case EPI_DW:
-      if (need > 2 * kT) return cudaErrorInvalidValue;
-      return launch_cfg<256, 6, 2 * kT, EPI_DW, 2>(a, st, num_sms);
-    case EPI_F32:
-      return launch_cfg<256, 4, kT, EPI_F32, 1>(a, st, num_sms);
-    default:
-      return cudaErrorInvalidValue;
-  }
 #else
-  switch (a.epi) {
     case EPI_SWIGLU_BWD:
       if (need > 2 * kT) return cudaErrorInvalidValue;
       return launch_cfg<256, 4, 2 * kT, EPI_SWIGLU_BWD, 1>(a, st, num_sms);
@@ -777,6 +773,7 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_s
     case EPI_STORE:
       if (need > 2 * kT) return cudaErrorInvalidValue;
       return launch_cfg<256, 4, 2 * kT, EPI_STORE, 1>(a, st, num_sms);
+#endif
     case EPI_F32:  // fp32 partial sums of a K split (decode-sized expert GEMMs)
       return launch_cfg<256, 4, kT, EPI_F32, 1>(a, st, num_sms);
     case EPI_DW:  // short-K tiles: the epilogue sets the pace, so eight epilogue warps (4 KB staging each)
@@ -785,7 +782,6 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int bn, cudaStream_t st, int num_s
     default:
       return cudaErrorInvalidValue;
   }
-#endif
 }
 
 }  // namespace moe

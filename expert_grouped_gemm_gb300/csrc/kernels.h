@@ -16,7 +16,7 @@ cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, in
 cudaError_t launch_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset, int* pad_off,
                               int* tile_off, int* chunk_base, int* pair_of_row, int* user_offsets, cudaStream_t st,
                               int* order = nullptr, int* tile_off2 = nullptr, int4* tile_rec = nullptr,
-                              int4* ord_rec = nullptr);
+                              int4* ord_rec = nullptr, int4* tile_rec2 = nullptr);
 cudaError_t launch_route_index(const uint64_t* masks, const int* chunk_base, const int* topk_idx, const int* offset,
                                const int* pad_off, int T, int E, int k, int* rowp_of_pair, int* row_of_pair,
                                int* pair_of_row, cudaStream_t st);
@@ -43,7 +43,8 @@ cudaError_t launch_splitk_swiglu(const float* part, int64_t stride, int S, const
                                  const int* pair_of_row, int F, void* ab, void* h, int num_sms, cudaStream_t st);
 cudaError_t launch_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off, int* ret_tile_off,
                             int* ret_src, int* user_offsets, cudaStream_t st, int* order = nullptr,
-                            int* ret_tile_off2 = nullptr, int4* tile_rec = nullptr, int4* ord_rec = nullptr);
+                            int* ret_tile_off2 = nullptr, int4* tile_rec = nullptr, int4* ord_rec = nullptr,
+                            int4* tile_rec2 = nullptr);
 cudaError_t launch_ret_index(const int* topk_idx, const int* rowp_of_pair, const int* row_of_pair,
                              const int* ret_cidx, const int* ret_offset, const int* ret_pad_off, int64_t P,
                              int* ret_src, int* crow_of_pair, int* ret_rows, int* user_rows, int num_sms,

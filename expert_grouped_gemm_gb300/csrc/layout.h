@@ -64,6 +64,8 @@ struct WsPtrs {
   int4* ord_rec;        // [E] experts in dW order: {expert, count, pad_off, 0}
   int4* ret_ord_rec;    // same for the kept rows
   float* part;          // fp32 partial sums of a K-split GEMM, split after split
+  int4* tile_rec2;      // [P/256 + E] per 256-row block (CTA-pair tiles): {expert, first row, count, pad_off}
+  int4* ret_tile_rec2;  // same for the kept rows
 };
 
 struct WsLayout {

@@ -120,6 +120,7 @@ WsLayout make_layout(const moe_dims* d) {
       (P / 128 + E + 1) * 16, (P / 128 + E + 1) * 16,  // tile_rec ret_tile_rec
       E * 16, E * 16,                                  // ord_rec ret_ord_rec
       L.part_elems * 4,                                // part
+      (P / 256 + E + 1) * 16, (P / 256 + E + 1) * 16,  // tile_rec2 ret_tile_rec2
   };
   L.n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   size_t off = 0;
@@ -138,7 +139,7 @@ const char* const kEntryNames[] = {
     "sh_y", "g", "score", "dy_perm", "ret_cidx", "ret_count", "ret_offset", "ret_pad_off", "ret_tile_off",
     "ret_src", "crow_of_pair", "ret_rows", "x_c", "ab_c", "h_c", "dy_c", "dab", "dx_pair", "dl", "dl_sel", "wrT",
     "sh_dab", "sh_dx", "order", "ret_order", "tile_off2", "ret_tile_off2", "tile_rec", "ret_tile_rec", "ord_rec",
-    "ret_ord_rec", "part"};
+    "ret_ord_rec", "part", "tile_rec2", "ret_tile_rec2"};
 
 WsPtrs make_ptrs(const WsLayout& L, void* ws) {
   char* b = static_cast<char*>(ws);
@@ -197,6 +198,8 @@ WsPtrs make_ptrs(const WsLayout& L, void* ws) {
   p.ord_rec = (int4*)nx();
   p.ret_ord_rec = (int4*)nx();
   p.part = (float*)nx();
+  p.tile_rec2 = (int4*)nx();
+  p.ret_tile_rec2 = (int4*)nx();
   return p;
 }
 
@@ -337,6 +340,7 @@ int expert_forward_gemms(const WsLayout& L, const WsPtrs& p, int bf, int sms, cu
     a.row_off = p.pad_off;
     a.tile_off = p.tile_off;
     a.tile_rec = p.tile_rec;
+    a.tile_rec2 = p.tile_rec2;
     a.tile_off2 = p.tile_off2;
     a.K = H;
     a.N = F;
@@ -379,6 +383,7 @@ int expert_forward_gemms(const WsLayout& L, const WsPtrs& p, int bf, int sms, cu
     a.row_off = p.pad_off;
     a.tile_off = p.tile_off;
     a.tile_rec = p.tile_rec;
+    a.tile_rec2 = p.tile_rec2;
     a.tile_off2 = p.tile_off2;
     a.K = F;
     a.N = H;
@@ -623,7 +628,7 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     CKL(launch_route_topk(p.logits, router_bias, T, E, k, p.topk_idx, p.topk_w, p.masks, st,
                           rks > 1 ? p.part : nullptr, rks, (int64_t)T * E));
     CKL(launch_route_scan(p.masks, (int)L.C, E, p.count, p.offset, p.pad_off, p.tile_off, p.chunk_base, p.pair_of_row,
-                         expert_offsets, st, p.order, p.tile_off2, p.tile_rec, p.ord_rec));
+                         expert_offsets, st, p.order, p.tile_off2, p.tile_rec, p.ord_rec, p.tile_rec2));
     CKL(launch_route_index(p.masks, p.chunk_base, p.topk_idx, p.offset, p.pad_off, T, E, k, p.rowp_of_pair,
                           p.row_of_pair, p.pair_of_row, st));
     if (bf)
@@ -697,7 +702,7 @@ int moe_select_retained(const moe_dims* dims, void* ws, size_t ws_bytes, void* s
                                   p.score, nullptr, scores, sms, st));
     CKL(launch_select(p.score, p.count, p.pad_off, quota, E, p.ret_cidx, p.ret_count, p.status, st));
     CKL(launch_ret_scan(p.ret_count, E, p.ret_offset, p.ret_pad_off, p.ret_tile_off, p.ret_src, retained_offsets, st,
-                        p.ret_order, p.ret_tile_off2, p.ret_tile_rec, p.ret_ord_rec));
+                        p.ret_order, p.ret_tile_off2, p.ret_tile_rec, p.ret_ord_rec, p.ret_tile_rec2));
     CKL(launch_ret_index(p.topk_idx, p.rowp_of_pair, p.row_of_pair, p.ret_cidx, p.ret_offset, p.ret_pad_off, L.P,
                         p.ret_src, p.crow_of_pair, p.ret_rows, retained_rows, sms, st));
     if (bf)
@@ -762,6 +767,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
   const int* toff = p.tile_off;
   const int* toff2 = p.tile_off2;
   const int4* trec = p.tile_rec;
+  const int4* trec2 = p.tile_rec2;
   const void* xs = p.x_perm;
   const void* abs_ = p.ab;
   const void* hs = p.h;
@@ -772,6 +778,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     roff = p.ret_pad_off;
     toff = p.ret_tile_off;
     trec = p.ret_tile_rec;
+    trec2 = p.ret_tile_rec2;
     toff2 = p.ret_tile_off2;
     xs = p.x_c;
     abs_ = p.ab_c;
@@ -805,6 +812,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.row_off = roff;
     a.tile_off = toff;
     a.tile_rec = trec;
+    a.tile_rec2 = trec2;
     a.tile_off2 = toff2;
     a.K = H;
     a.N = F;
@@ -833,6 +841,7 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     a.row_off = roff;
     a.tile_off = toff;
     a.tile_rec = trec;
+    a.tile_rec2 = trec2;
     a.tile_off2 = toff2;
     a.K = 2 * F;
     a.N = H;

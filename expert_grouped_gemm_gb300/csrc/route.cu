@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* 
 __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset,
                                                      int* pad_off, int* tile_off, int* chunk_base, int* pair_of_row,
                                                      int* user_offsets, int* order, int* tile_off2,
-                                                     int4* tile_rec, int4* ord_rec) {
+                                                     int4* tile_rec, int4* ord_rec, int4* tile_rec2) {
   __shared__ int part_cnt[1024];
   int parts = 1;
   while (parts * 2 * E <= 1024) parts *= 2;
@@ -194,6 +194,8 @@ __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int 
     for (int r = op + cnt; r < op + pad; ++r) pair_of_row[r] = -1;
     if (tile_rec)
       for (int j = 0; j < tiles; ++j) tile_rec[ot + j] = make_int4(e, j * 128, cnt, op);
+    if (tile_rec2)
+      for (int j = 0; j < tiles2; ++j) tile_rec2[ot2 + j] = make_int4(e, j * 256, cnt, op);
     if (ord_rec && order) ord_rec[rank] = make_int4(e, cnt, op, 0);
   }
   if (e == 0) {
@@ -427,9 +429,9 @@ cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, in
 
 cudaError_t launch_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset, int* pad_off,
                               int* tile_off, int* chunk_base, int* pair_of_row, int* user_offsets, cudaStream_t st,
-                              int* order, int* tile_off2, int4* tile_rec, int4* ord_rec) {
+                              int* order, int* tile_off2, int4* tile_rec, int4* ord_rec, int4* tile_rec2) {
   k_route_scan<<<1, 1024, 0, st>>>(masks, C, E, count, offset, pad_off, tile_off, chunk_base, pair_of_row,
-                                   user_offsets, order, tile_off2, tile_rec, ord_rec);
+                                   user_offsets, order, tile_off2, tile_rec, ord_rec, tile_rec2);
   return cudaGetLastError();
 }
 

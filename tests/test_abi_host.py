@@ -152,7 +152,8 @@ def test_full_bwd_requires_gradient_pointers(lib):
 
 
 def test_cta_pair_variant_compiles():
-    """The CTA-pair (cta_group::2) grouped GEMM, kept as a build option, still compiles for sm_103a."""
+    """The CTA-pair (cta_group::2) variable-M grouped GEMM, kept as a build option beside
+    the default single CTAs, still compiles for sm_103a."""
     import shutil
     import subprocess
 
@@ -164,7 +165,7 @@ def test_cta_pair_variant_compiles():
     src = os.path.join(b.CSRC, "gemm_tc.cu")
     os.makedirs(b.BUILD, exist_ok=True)  # in-tree build folder (ignored by git)
     obj = os.path.join(b.BUILD, "gemm_tc_pair_check.o")
-    r = subprocess.run([nvcc, *b.ARCH, *b.FLAGS, "-DMOE_GEMM_CTAS=2", "-c", src, "-o", obj], capture_output=True,
+    r = subprocess.run([nvcc, *b.ARCH, *b.FLAGS, "-DMOE_VARM_CTAS=2", "-c", src, "-o", obj], capture_output=True,
                        text=True)
     assert r.returncode == 0, r.stderr[-2000:]
     os.remove(obj)
