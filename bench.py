@@ -488,12 +488,77 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "copies": "pinned host buffers; on a second stream, overlapped with the neighbouring steps"},
             "roofline": roof}
+    if world == 1:
+        line["decode"] = decode_leg(w, inp, dev, peaks)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, args.seed, args.cpu_budget_s)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def decode_leg(w, inp, dev, peaks, calls: int = 50) -> dict | None:
+    """Per-call GPU time of the forward at decode-sized token counts, fused (moe_fwd_decode)
+    and unfused (moe_fwd), on the same layer's weights, beside the weight-streaming floor:
+    the bytes of the experts the tokens touch (plus the router) at the measured HBM rate.
+    Each is timed over one CUDA-graph replay of `calls` calls."""
+    import torch
+
+    from expert_grouped_gemm_gb300 import _lib
+    from expert_grouped_gemm_gb300.inputs import custom
+    from expert_grouped_gemm_gb300.layer import MoELayer
+
+    if w.dtype != "bf16" or w.E > 256 or w.k > 16 or max(w.H, w.F, w.F_shared) > 4096:
+        return None
+    out = {}
+    for T in (1, 8):
+        wd = custom(f"{w.name}_decode_t{T}", T=T, H=w.H, F=w.F, E=w.E, k=w.k, F_shared=w.F_shared, zipf_s=w.zipf_s,
+                    zero_experts=w.zero_experts)
+        layer = MoELayer(wd, inp, dev, record_routing=True)
+        x = inp["x"][:T].to(dev).contiguous()
+        times, how = {}, {}
+        for name, fn in (("fused", layer.forward_decode), ("unfused", layer.forward)):
+            for _ in range(5):
+                fn(x)
+            torch.cuda.synchronize()
+            # GPU time per call: the calls replayed from a CUDA graph, so host-side call
+            # overhead (argument checks, tensor-map encoding, launches) is not counted;
+            # eager back-to-back calls if the capture is refused
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            try:
+                s = torch.cuda.Stream(device=dev)
+                s.wait_stream(torch.cuda.current_stream())
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=s):
+                    for _ in range(calls):
+                        fn(x, stream=s)
+                graph.replay()
+                torch.cuda.synchronize()
+                e0.record()
+                graph.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                how[name] = "cuda graph replay"
+                del graph
+            except Exception as exc:  # noqa: BLE001 - report and fall back
+                torch.cuda.synchronize()
+                how[name] = f"eager (graph capture failed: {type(exc).__name__})"
+                e0.record()
+                for _ in range(calls):
+                    fn(x)
+                e1.record()
+                torch.cuda.synchronize()
+            times[name] = e0.elapsed_time(e1) / calls * 1e3
+        if _lib.moe_read_status(layer.ws) != 0:
+            raise RuntimeError("device status not OK in the decode leg")
+        touched = int(torch.unique(layer.topk_idx).numel())
+        wbytes = 2 * (touched * 3 * w.H * w.F + 3 * w.H * w.F_shared + w.H * w.E)
+        floor = wbytes / (float(peaks["hbm_gbs"]) * 1e9) * 1e6
+        out[f"T{T}"] = {"fused_us": times["fused"], "unfused_us": times["unfused"], "timing": how, "experts_touched": touched,
+                        "weight_bytes": wbytes, "floor_us": floor, "fused_over_floor": times["fused"] / floor}
+        del layer
+    return out
 
 
 def kernel_hash() -> str:

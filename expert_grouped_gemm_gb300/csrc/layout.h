@@ -66,6 +66,7 @@ struct WsPtrs {
   float* part;          // fp32 partial sums of a K-split GEMM, split after split
   int4* tile_rec2;      // [P/256 + E] per 256-row block (CTA-pair tiles): {expert, first row, count, pad_off}
   int4* ret_tile_rec2;  // same for the kept rows
+  void* decode;         // scratch of the fused decode forward (T <= 16 only; empty otherwise)
 };
 
 struct WsLayout {

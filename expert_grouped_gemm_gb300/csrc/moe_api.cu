@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "decode.h"
 #include "gemm_launch.h"
 #include "kernels.h"
 #include "layout.h"
@@ -121,6 +122,9 @@ WsLayout make_layout(const moe_dims* d) {
       E * 16, E * 16,                                  // ord_rec ret_ord_rec
       L.part_elems * 4,                                // part
       (P / 256 + E + 1) * 16, (P / 256 + E + 1) * 16,  // tile_rec2 ret_tile_rec2
+      (int64_t)(d->dtype == MOE_BF16 && decode_supported(T, H, F, E, k, Fs)  // decode scratch (T <= 16)
+                    ? decode_scratch_bytes(T, H, F, E, Fs)
+                    : 0),
   };
   L.n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   size_t off = 0;
@@ -139,7 +143,7 @@ const char* const kEntryNames[] = {
     "sh_y", "g", "score", "dy_perm", "ret_cidx", "ret_count", "ret_offset", "ret_pad_off", "ret_tile_off",
     "ret_src", "crow_of_pair", "ret_rows", "x_c", "ab_c", "h_c", "dy_c", "dab", "dx_pair", "dl", "dl_sel", "wrT",
     "sh_dab", "sh_dx", "order", "ret_order", "tile_off2", "ret_tile_off2", "tile_rec", "ret_tile_rec", "ord_rec",
-    "ret_ord_rec", "part", "tile_rec2", "ret_tile_rec2"};
+    "ret_ord_rec", "part", "tile_rec2", "ret_tile_rec2", "decode"};
 
 WsPtrs make_ptrs(const WsLayout& L, void* ws) {
   char* b = static_cast<char*>(ws);
@@ -200,6 +204,7 @@ WsPtrs make_ptrs(const WsLayout& L, void* ws) {
   p.part = (float*)nx();
   p.tile_rec2 = (int4*)nx();
   p.ret_tile_rec2 = (int4*)nx();
+  p.decode = nx();
   return p;
 }
 
@@ -663,6 +668,45 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
   s.ws_gate = ws_gate;
   s.ws_up = ws_up;
   s.ws_down = ws_down;
+  return MOE_OK;
+}
+
+int moe_fwd_decode(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const void* x, const void* w_router,
+                   const float* router_bias, const void* w_gate, const void* w_up, const void* w_down,
+                   const void* ws_gate, const void* ws_up, const void* ws_down, void* y, int32_t* topk_idx,
+                   float* topk_w, float* logits) {
+  WsLayout L;
+  int rc = check_ws(dims, ws, ws_bytes, &L);
+  if (rc) return rc;
+  if (dims->dtype != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "moe_fwd_decode: bf16 only");
+  if (!decode_supported(L.T, L.H, L.F, L.E, L.k, L.Fs))
+    return fail(MOE_ERR_UNSUPPORTED,
+                "moe_fwd_decode: needs T <= 16, E <= 256, k <= 16 and H, F, F_shared <= 4096 (T=%lld E=%lld k=%lld)",
+                (long long)L.T, (long long)L.E, (long long)L.k);
+  const bool shared = dims->F_shared > 0;
+  if ((rc = check_ptr(x, "x", true)) || (rc = check_ptr(w_router, "w_router", true)) ||
+      (rc = check_ptr(router_bias, "router_bias", false, 4)) || (rc = check_ptr(w_gate, "w_gate", true)) ||
+      (rc = check_ptr(w_up, "w_up", true)) || (rc = check_ptr(w_down, "w_down", true)) ||
+      (rc = check_ptr(y, "y", true)) || (rc = check_ptr(topk_idx, "topk_idx", false, 4)) ||
+      (rc = check_ptr(topk_w, "topk_w", false, 4)) || (rc = check_ptr(logits, "logits", false, 4)))
+    return rc;
+  if (shared) {
+    if ((rc = check_ptr(ws_gate, "ws_gate", true)) || (rc = check_ptr(ws_up, "ws_up", true)) ||
+        (rc = check_ptr(ws_down, "ws_down", true)))
+      return rc;
+  } else if (ws_gate || ws_up || ws_down) {
+    return fail(MOE_ERR_INVALID_ARG, "shared-expert weights given but F_shared == 0");
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WsPtrs p = make_ptrs(L, ws);
+  CK(cudaMemsetAsync(p.status, 0, sizeof(int), st));
+  g_launches += 1;
+  CK(launch_decode_fwd((int)L.T, (int)L.H, (int)L.F, (int)L.E, (int)L.k, (int)L.Fs, x, w_router, router_bias, w_gate,
+                       w_up, w_down, ws_gate, ws_up, ws_down, y, p.topk_idx, p.topk_w, topk_idx, topk_w, logits,
+                       p.decode, p.status, num_sms_current(), st));
+  // inference only: the routing buffers no longer hold a forward the backward could use
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_state[ws] = State();
   return MOE_OK;
 }
 

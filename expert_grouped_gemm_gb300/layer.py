@@ -68,6 +68,16 @@ class MoELayer:
                      self.row_of_pair if r else None, self.logits if r else None, stream=stream)
         return self.y
 
+    def forward_decode(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+        """Inference forward through the fused decode kernel (1 <= T <= 16, bf16)."""
+        p = self.p
+        r = self.record
+        _lib.moe_fwd_decode(self.dims, self.ws, x, p["w_router"], p["router_bias"], p["w_gate"], p["w_up"],
+                            p["w_down"], p["ws_gate"], p["ws_up"], p["ws_down"], self.y,
+                            self.topk_idx if r else None, self.topk_w if r else None, self.logits if r else None,
+                            stream=stream)
+        return self.y
+
     def select(self, dy: torch.Tensor, quota: torch.Tensor | None, stream=None) -> None:
         r = self.record
         _lib.moe_select_retained(self.dims, self.ws, dy, quota, self.ret_offsets if r else None,

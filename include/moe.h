@@ -122,6 +122,30 @@ MOE_API int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* strea
             int32_t* row_of_pair, float* logits);
 
 /*
+ * moe_fwd_decode -- the forward of moe_fwd for decode-sized token counts, fused into
+ * one persistent kernel, for inference ([I14] Evidence: per-token latency with 1..8
+ * routed experts at inference time). At a handful of tokens the layer is a weight
+ * stream; this call reads each touched expert's W_gate, W_up and W_down from HBM once,
+ * with no other launch than its own.
+ *   Computes what moe_fwd computes: y, and optionally the top-k experts, weights and
+ *   the biased fp32 router logits the selection used. The router logits are summed in
+ *   another order than moe_fwd's, so an index can differ from moe_fwd's at a near tie.
+ * Needs dims.dtype == MOE_BF16, 1 <= T <= 16, E <= 256, k <= 16 and H, F,
+ * F_shared <= 4096; other dims return MOE_ERR_UNSUPPORTED (use moe_fwd).
+ * Inputs and outputs as moe_fwd (y[T,H]; topk_idx[T,k] int32, topk_w[T,k] float,
+ * logits[T,E] float nullable). The workspace is the one moe_workspace_size() gives
+ * for these dims. Nothing is kept for a backward: moe_select_retained / moe_bwd on
+ * this workspace return MOE_ERR_STATE until the next moe_fwd.
+ * Every wait inside the kernel is bounded; one that runs out writes MOE_ERR_TIMEOUT
+ * to the workspace status word (moe_read_status).
+ */
+MOE_API int moe_fwd_decode(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream,
+                           const void* x, const void* w_router, const float* router_bias,
+                           const void* w_gate, const void* w_up, const void* w_down,
+                           const void* ws_gate, const void* ws_up, const void* ws_down,
+                           void* y, int32_t* topk_idx, float* topk_w, float* logits);
+
+/*
  * moe_select_retained -- per-pair scores and per-expert quota selection with
  * physical compaction ([LRMoE] Abstract: a per-pair estimate of the
  * contribution to the expert update, pairs selected within per-expert
