@@ -498,11 +498,13 @@ def run_ours(args):
     return 0
 
 
-def decode_leg(w, inp, dev, peaks, calls: int = 50) -> dict | None:
+def decode_leg(w, inp, dev, peaks, calls: int = 48, layers: int = 4) -> dict | None:
     """Per-call GPU time of the forward at decode-sized token counts, fused (moe_fwd_decode)
-    and unfused (moe_fwd), on the same layer's weights, beside the weight-streaming floor:
-    the bytes of the experts the tokens touch (plus the router) at the measured HBM rate.
-    Each is timed over one CUDA-graph replay of `calls` calls."""
+    and unfused (moe_fwd), beside the weight-streaming floor: the bytes of the experts the
+    tokens touch (plus the router) at the measured HBM rate. The calls cycle through
+    `layers` copies of the layer's weights, as consecutive layers of a model would, so a
+    call finds no weight of the previous one in L2 (4 x the touched bytes > 129 MB at
+    T=1). Each is timed over one CUDA-graph replay of `calls` calls."""
     import torch
 
     from expert_grouped_gemm_gb300 import _lib
@@ -515,12 +517,14 @@ def decode_leg(w, inp, dev, peaks, calls: int = 50) -> dict | None:
     for T in (1, 8):
         wd = custom(f"{w.name}_decode_t{T}", T=T, H=w.H, F=w.F, E=w.E, k=w.k, F_shared=w.F_shared, zipf_s=w.zipf_s,
                     zero_experts=w.zero_experts)
-        layer = MoELayer(wd, inp, dev, record_routing=True)
+        stack = [MoELayer(wd, inp, dev, record_routing=True) for _ in range(layers)]
         x = inp["x"][:T].to(dev).contiguous()
         times, how = {}, {}
-        for name, fn in (("fused", layer.forward_decode), ("unfused", layer.forward)):
-            for _ in range(5):
-                fn(x)
+        for name in ("fused", "unfused"):
+            fns = [(lay.forward_decode if name == "fused" else lay.forward) for lay in stack]
+            for _ in range(3):
+                for fn in fns:
+                    fn(x)
             torch.cuda.synchronize()
             # GPU time per call: the calls replayed from a CUDA graph, so host-side call
             # overhead (argument checks, tensor-map encoding, launches) is not counted;
@@ -531,8 +535,8 @@ def decode_leg(w, inp, dev, peaks, calls: int = 50) -> dict | None:
                 s.wait_stream(torch.cuda.current_stream())
                 graph = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(graph, stream=s):
-                    for _ in range(calls):
-                        fn(x, stream=s)
+                    for c in range(calls):
+                        fns[c % layers](x, stream=s)
                 graph.replay()
                 torch.cuda.synchronize()
                 e0.record()
@@ -545,19 +549,21 @@ def decode_leg(w, inp, dev, peaks, calls: int = 50) -> dict | None:
                 torch.cuda.synchronize()
                 how[name] = f"eager (graph capture failed: {type(exc).__name__})"
                 e0.record()
-                for _ in range(calls):
-                    fn(x)
+                for c in range(calls):
+                    fns[c % layers](x)
                 e1.record()
                 torch.cuda.synchronize()
             times[name] = e0.elapsed_time(e1) / calls * 1e3
-        if _lib.moe_read_status(layer.ws) != 0:
-            raise RuntimeError("device status not OK in the decode leg")
-        touched = int(torch.unique(layer.topk_idx).numel())
+        for lay in stack:
+            if _lib.moe_read_status(lay.ws) != 0:
+                raise RuntimeError("device status not OK in the decode leg")
+        touched = int(torch.unique(stack[0].topk_idx).numel())
         wbytes = 2 * (touched * 3 * w.H * w.F + 3 * w.H * w.F_shared + w.H * w.E)
         floor = wbytes / (float(peaks["hbm_gbs"]) * 1e9) * 1e6
         out[f"T{T}"] = {"fused_us": times["fused"], "unfused_us": times["unfused"], "timing": how, "experts_touched": touched,
-                        "weight_bytes": wbytes, "floor_us": floor, "fused_over_floor": times["fused"] / floor}
-        del layer
+                        "weight_bytes": wbytes, "floor_us": floor, "fused_over_floor": times["fused"] / floor,
+                        "layers_cycled": layers}
+        del stack
     return out
 
 

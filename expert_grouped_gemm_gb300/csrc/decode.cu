@@ -6,8 +6,8 @@
 // short kernels whose launch, prologue and pipeline fill cost more than the stream.
 // Here one cooperative launch (one CTA per SM, every CTA resident) runs four phases
 // separated by grid-wide barriers:
-//   R  router logits: CTA b computes logits[t, 8b .. 8b+7] over all of H (CUDA cores),
-//      with the bias added;
+//   R  router logits: CTA b computes logits[t, b], logits[t, b + G], ... over all of H
+//      (CUDA cores), with the bias added;
 //   G  every CTA takes the top-k and the renormalised softmax weights of every token
 //      and builds the same slot table (the routed (token, expert) pairs sorted by
 //      expert then token, then one slot per token for the shared expert); then units
@@ -35,14 +35,12 @@ namespace moe {
 constexpr int kDecMaxT = 16;      // tokens (the mma M dimension)
 constexpr int kDecThreads = 256;  // 8 warps: one 8-column n-tile of a 64-column unit each
 constexpr int kDecStepRows = 256; // weight rows per ring step: four 64-row boxes
-constexpr int kDecBufs = 4;       // weight tiles in flight per CTA
+constexpr int kDecBufs = 6;       // weight tiles in flight per CTA
 constexpr int kDecBoxRows = 64;
 constexpr int kDecTileBytes = kDecStepRows * 128;            // 32 KB: 256 rows x 64 bf16
 constexpr int kDecALd = kDecStepRows + 8;                    // A tile row stride (elements), padded
 constexpr int kDecMaxE = 256;
 constexpr int kDecMaxK = 16;  // T * k <= 256: one thread per routed pair when ranking them
-constexpr int kDecMaxSlots = kDecMaxT * kDecMaxK + kDecMaxT;  // routed pairs + shared-expert tokens
-constexpr int kDecRouterE = 8;                                // experts per router unit
 constexpr int kDecMaxH = 4096;
 constexpr uint64_t kDecWaitNs = 1000000000ull;                // 1 s
 
@@ -60,13 +58,15 @@ struct DecodeArgs {
   float* logits;      // [T][E] biased fp32 logits
   __nv_bfloat16* hbuf;  // [slots][Fm]
   float* ypair;       // [slots][H]
+  float* part_g;      // [H / 256][slots][gate, up][Fm]: x Wg and x Wu over one 256-row chunk of H
+  int smax;           // slot rows of part_g: T * k + T
   unsigned* sync;     // grid barrier counter (zeroed before the launch)
   int* status;
 };
 
 struct DecodeShared {
   __nv_bfloat16 a_tile[kDecMaxT * kDecALd];  // tokens x rows of the current step
-  float red[32][kDecMaxT][kDecRouterE];      // router: partial sums of 32 row groups
+  float red[kDecThreads / 32][kDecMaxT];     // router: one partial sum per warp and token
   int s_idx[kDecMaxT * kDecMaxK];
   float s_w[kDecMaxT * kDecMaxK];
   int slot_pair[kDecMaxT * kDecMaxK];        // routed slot -> pair t*k + j
@@ -102,15 +102,19 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
-// Grid-wide barrier number `phase` (1, 2, ...): every CTA arrives once; returns false
-// when the wait ran out (or an earlier wait did), after recording MOE_ERR_TIMEOUT.
-__device__ bool dec_grid_sync(const DecodeArgs& a, DecodeShared& sh, unsigned phase) {
+// Grid-wide barrier number `phase` (1, 2, ...), in two halves so that a CTA can issue
+// work between them: arrive (every CTA once: a release add after the CTA's own barrier)
+// and wait (thread 0 polls with acquire loads). wait returns false when the wait ran
+// out (or an earlier one did), after recording MOE_ERR_TIMEOUT.
+__device__ __forceinline__ void dec_grid_arrive(const DecodeArgs& a, DecodeShared& sh) {
   __syncthreads();
-  if (threadIdx.x == 0) {
-    if (!sh.abort_flag) {
-      __threadfence();
-      atomicAdd(a.sync, 1u);
-      const unsigned target = phase * gridDim.x;
+  if (threadIdx.x == 0 && !sh.abort_flag)
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a.sync), "r"(1u) : "memory");
+}
+__device__ bool dec_grid_wait(const DecodeArgs& a, DecodeShared& sh, unsigned phase) {
+  if (threadIdx.x == 0 && !sh.abort_flag) {
+    const unsigned target = phase * gridDim.x;
+    if (ld_acquire_gpu(a.sync) < target) {
       const uint64_t t0 = globaltimer_ns();
       while (ld_acquire_gpu(a.sync) < target) {
         if (globaltimer_ns() - t0 > kDecWaitNs) {
@@ -118,129 +122,103 @@ __device__ bool dec_grid_sync(const DecodeArgs& a, DecodeShared& sh, unsigned ph
           set_status(a.status, MOE_ERR_TIMEOUT);
           break;
         }
-        __nanosleep(32);
       }
-      __threadfence();
     }
   }
   __syncthreads();
   return !sh.abort_flag;
 }
+__device__ __forceinline__ bool dec_grid_sync(const DecodeArgs& a, DecodeShared& sh, unsigned phase) {
+  dec_grid_arrive(a, sh);
+  return dec_grid_wait(a, sh, phase);
+}
 
-// d += (sh.a_tile, nrows columns) x (weight tile at wt, nrows rows x 64 columns): warp w
-// takes the 16 x 8 block of columns 8w .. 8w+7 (rows = tokens).
-__device__ __forceinline__ void step_mma(const DecodeShared& sh, uint32_t wt, int nrows, float (&d)[4]) {
+// d0 + d1 += (sh.a_tile, nrows columns) x (weight tile at wt, nrows rows x 64 columns):
+// warp w takes the 16 x 8 block of columns 8w .. 8w+7 (rows = tokens). Even 16-row
+// slices go to d0, odd ones to d1, so two mma chains are in flight; nrows is a multiple
+// of 64.
+__device__ __forceinline__ void step_mma(const DecodeShared& sh, uint32_t wt, int nrows, float (&d0)[4],
+                                         float (&d1)[4]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t a_base = smem_u32(sh.a_tile);
-#pragma unroll 4
-  for (int kk = 0; kk < nrows; kk += 16) {
-    uint32_t a0, a1, a2, a3, b0, b1;
+#pragma unroll 2
+  for (int kk = 0; kk < nrows; kk += 32) {
+    uint32_t a0, a1, a2, a3, b0, b1, c0, c1, c2, c3, e0, e1;
     // A: matrices (rows 0-7, k 0-7), (8-15, 0-7), (0-7, 8-15), (8-15, 8-15)
     const int ar = lane & 15, ak = kk + ((lane >> 4) << 3);
     ldsm_x4(a_base + (uint32_t)((ar * kDecALd + ak) * 2), a0, a1, a2, a3);
+    ldsm_x4(a_base + (uint32_t)((ar * kDecALd + ak + 16) * 2), c0, c1, c2, c3);
     // B: weight rows kk..kk+15, columns 8w..8w+7 (16-byte chunk w of each swizzled row)
-    const int br = kk + (lane & 15);
+    const int br = kk + (lane & 15), br2 = br + 16;
     ldsm_x2_trans(wt + (uint32_t)(br * 128 + ((warp ^ (br & 7)) << 4)), b0, b1);
-    mma_16816(d, a0, a1, a2, a3, b0, b1);
+    ldsm_x2_trans(wt + (uint32_t)(br2 * 128 + ((warp ^ (br2 & 7)) << 4)), e0, e1);
+    mma_16816(d0, a0, a1, a2, a3, b0, b1);
+    mma_16816(d1, c0, c1, c2, c3, e0, e1);
   }
 }
 
-// A weight-streaming phase: this CTA's units (blockIdx.x + li * gridDim.x < nunits), each
-// a sequence of steps; step (unit i, s) is a tile of at most 256 weight rows x 64 columns
-// (step_info: tensor map, first row, column, rows) that meets the A tile of the unit's
-// tokens (needs_a(i, s): the step starts a new A tile; load_a / store_a move it through
-// registers one A tile ahead). Four weight tiles are in flight. mma(i, s, wt, nrows)
-// accumulates; done(i) writes the unit's result. Returns false after a wait ran out.
-template <typename NSteps, typename StepInfo, typename NeedsA, typename LoadA, typename StoreA, typename Mma,
-          typename Done>
-__device__ bool stream_steps(DecodeShared& sh, uint8_t* tiles, uint32_t (&bar_phase)[kDecBufs], int nunits,
-                             const DecodeArgs& a, NSteps nsteps, StepInfo step_info, NeedsA needs_a, LoadA load_a,
-                             StoreA store_a, Mma mma, Done done) {
-  const int G = gridDim.x;
-  const int mine = nunits > (int)blockIdx.x ? (nunits - (int)blockIdx.x + G - 1) / G : 0;
-  if (mine == 0) return true;
-  auto unit = [&](int li) { return (int)blockIdx.x + li * G; };
-  // cursor over this CTA's steps
-  struct Cur {
-    int li, s;
-  };
-  auto advance = [&](Cur& c) {
-    if (++c.s >= nsteps(unit(c.li))) {
-      c.s = 0;
-      ++c.li;
-    }
-  };
-  int slot_b = 0;  // ring slot of the next step to issue
-  auto issue = [&](const Cur& c) {  // thread 0: the weight boxes of step c
-    const CUtensorMap* map;
-    int row0, col0, nrows;
-    step_info(unit(c.li), c.s, map, row0, col0, nrows);
-    const int b = slot_b;
-    slot_b = (slot_b + 1) % kDecBufs;
+// The weight ring: kDecBufs shared-memory tiles of at most 256 rows x 64 columns, filled
+// by TMA in issue order and consumed in the same order. Every thread keeps the same copy
+// of this state; thread 0 issues the copies.
+struct Ring {
+  int next_issue, next_use, inflight;
+  uint32_t phase[kDecBufs];
+};
+
+__device__ __forceinline__ void ring_issue(DecodeShared& sh, uint8_t* tiles, Ring& r, const CUtensorMap* map,
+                                           int row0, int col0, int nrows) {
+  const int b = r.next_issue;
+  r.next_issue = (b + 1) % kDecBufs;
+  ++r.inflight;
+  if (threadIdx.x == 0) {
     const int nbox = (nrows + kDecBoxRows - 1) / kDecBoxRows;
-    if (nbox == 0) {
-      mbar_arrive(&sh.bar[b]);
-      return;
-    }
     fence_async_smem();  // this CTA's earlier reads of the buffer come before the copy
     mbar_arrive_expect_tx(&sh.bar[b], (uint32_t)(nbox * kDecBoxRows * 128));
     for (int x = 0; x < nbox; ++x)
       tma_load_2d(smem_u32(tiles + b * kDecTileBytes + x * kDecBoxRows * 128), map, smem_u32(&sh.bar[b]), col0,
                   row0 + x * kDecBoxRows);
-  };
-  Cur ic{0, 0}, cc{0, 0}, ac{0, 0};  // issue, consume and A-load cursors
-  int inflight = 0;
-  if (threadIdx.x == 0)
-    for (; inflight < kDecBufs && ic.li < mine; ++inflight, advance(ic)) issue(ic);
-  __syncwarp();
-  // every thread keeps the same issue cursor (thread 0 issued)
-  if (threadIdx.x != 0)
-    for (int q = 0; q < kDecBufs && ic.li < mine; ++q) advance(ic), ++inflight;
-  uint4 av[2];
-  load_a(unit(ac.li), ac.s, av);  // the first step always starts an A tile
-  int b = 0;
-  while (cc.li < mine) {
-    const int i = unit(cc.li);
-    if (needs_a(i, cc.s)) {
-      store_a(av);  // the previous readers of the A tile passed the last barrier
-      // the next step that starts an A tile, in flight during this one
-      do advance(ac); while (ac.li < mine && !needs_a(unit(ac.li), ac.s));
-      if (ac.li < mine) load_a(unit(ac.li), ac.s, av);
-    }
-    const bool landed = mbar_wait_bounded(&sh.bar[b], bar_phase[b], (volatile int*)&sh.abort_flag, kDecWaitNs);
-    if (landed)
-      bar_phase[b] ^= 1u;
-    else
-      set_status(a.status, MOE_ERR_TIMEOUT);
-    __syncthreads();
-    if (sh.abort_flag) {
-      // let this CTA's copies still in flight land before its shared memory is released
-      // (the pending phase of each buffer; this step's own only if it has not landed)
-      if (threadIdx.x == 0)
-        for (int q = landed ? 1 : 0; q < inflight; ++q) {
-          const int bq = (b + q) % kDecBufs;
-          mbar_wait_timed(&sh.bar[bq], bar_phase[bq], 200000000ull);
-        }
-      __syncthreads();
-      return false;
-    }
-    const CUtensorMap* map;
-    int row0, col0, nrows;
-    step_info(i, cc.s, map, row0, col0, nrows);
-    mma(i, cc.s, smem_u32(tiles + b * kDecTileBytes), nrows);
-    const bool last = cc.s + 1 >= nsteps(i);
-    if (last) done(i);
-    __syncthreads();  // this buffer (and, at an A step, the A tile) is free again
-    --inflight;
-    if (ic.li < mine) {
-      if (threadIdx.x == 0) issue(ic);
-      advance(ic);
-      ++inflight;
-    }
-    b = (b + 1) % kDecBufs;
-    advance(cc);
   }
+}
+
+// Waits for the oldest tile in flight and returns its shared-memory address in wt; false
+// after a wait ran out, once this CTA's other copies in flight have landed (so that its
+// shared memory may be released).
+__device__ __forceinline__ bool ring_wait(DecodeShared& sh, uint8_t* tiles, Ring& r, const DecodeArgs& a,
+                                          uint32_t& wt) {
+  const int b = r.next_use;
+  const bool landed = mbar_wait_bounded(&sh.bar[b], r.phase[b], (volatile int*)&sh.abort_flag, kDecWaitNs);
+  if (landed)
+    r.phase[b] ^= 1u;
+  else
+    set_status(a.status, MOE_ERR_TIMEOUT);
+  __syncthreads();
+  if (sh.abort_flag) {
+    if (threadIdx.x == 0)
+      for (int q = landed ? 1 : 0; q < r.inflight; ++q) {
+        const int bq = (b + q) % kDecBufs;
+        mbar_wait_timed(&sh.bar[bq], r.phase[bq], 200000000ull);
+      }
+    __syncthreads();
+    return false;
+  }
+  wt = smem_u32(tiles + b * kDecTileBytes);
   return true;
+}
+
+// After the barrier that ends the step: the oldest tile's buffer is free again.
+__device__ __forceinline__ void ring_release(Ring& r) {
+  r.next_use = (r.next_use + 1) % kDecBufs;
+  --r.inflight;
+}
+
+// A tile of the current step: up to 16 rows (the unit's tokens) x 256 columns, two
+// 16-byte pieces per thread, staged in registers one tile ahead.
+__device__ __forceinline__ void a_store(DecodeShared& sh, const uint4 (&v)[2]) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int idx = threadIdx.x + q * kDecThreads, r = idx >> 5, c = idx & 31;
+    *reinterpret_cast<uint4*>(sh.a_tile + r * kDecALd + c * 8) = v[q];
+  }
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -264,107 +242,104 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     fence_mbar_init();
   }
   __syncthreads();
-  uint32_t bar_phase[kDecBufs] = {0, 0, 0, 0};
 
   // ---------------------------------------------------------------- R: router logits
-  {
-    // x[T][H] staged in the (still idle) weight ring: at most 16 x 4096 bf16 = 128 KB
-    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(tiles);
-    const int EB = (E + kDecRouterE - 1) / kDecRouterE;
-    if ((int)blockIdx.x < EB) {
-      for (int i = tid; i < T * (H / 8); i += kDecThreads)
-        reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(a.x)[i];
-      __syncthreads();
-    }
-    for (int eb = blockIdx.x; eb < EB; eb += G) {
-      // thread: expert ec of the block, rows rg, rg + 32, ... (loads of 16 rows in flight)
-      const int ec = tid & (kDecRouterE - 1), rg = tid / kDecRouterE, e = eb * kDecRouterE + ec;
-      float acc[kDecMaxT];
+  // CTA b takes experts b, b + G, ...; thread i the rows 8i .. 8i+7 of each 2048-row
+  // stretch of H (one column element of W_router per row, a 16-byte load of x per token)
+  for (int e = blockIdx.x; e < E; e += G) {
+    float acc[kDecMaxT];
 #pragma unroll
-      for (int t = 0; t < kDecMaxT; ++t) acc[t] = 0.0f;
-      for (int r0 = rg; r0 < H; r0 += 32 * 16) {
-        float wv[16];
+    for (int t = 0; t < kDecMaxT; ++t) acc[t] = 0.0f;
+    for (int r0 = tid * 8; r0 < H; r0 += kDecThreads * 8) {
+      float wv[8];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int r = r0 + 32 * q;
-          wv[q] = (e < E && r < H) ? __bfloat162float(a.w_router[(int64_t)r * E + e]) : 0.0f;
-        }
+      for (int q = 0; q < 8; ++q) wv[q] = __bfloat162float(a.w_router[(int64_t)(r0 + q) * E + e]);
+      uint4 xr[kDecMaxT];  // every token's 16 bytes in flight before the sums
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int r = r0 + 32 * q;
-          if (r < H) {
+      for (int t = 0; t < kDecMaxT; ++t)
+        xr[t] = t < T ? *reinterpret_cast<const uint4*>(a.x + (int64_t)t * H + r0) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int t = 0; t < kDecMaxT; ++t)
-              if (t < T) acc[t] = fmaf(__bfloat162float(xs[t * H + r]), wv[q], acc[t]);
-          }
-        }
+      for (int t = 0; t < kDecMaxT; ++t) {
+        float xv[8];
+        bf16x8_to_f(xr[t], xv);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[t] = fmaf(xv[q], wv[q], acc[t]);
       }
-#pragma unroll
-      for (int t = 0; t < kDecMaxT; ++t) sh.red[rg][t][ec] = acc[t];
-      __syncthreads();
-      if (tid < T * kDecRouterE) {  // the 32 row groups added in order, then the bias
-        const int t = tid / kDecRouterE, c = tid % kDecRouterE, ee = eb * kDecRouterE + c;
-        float l = 0.0f;
-        for (int g = 0; g < 32; ++g) l += sh.red[g][t][c];
-        if (ee < E) {
-          l += a.bias ? a.bias[ee] : 0.0f;
-          a.logits[t * E + ee] = l;
-          if (a.user_logits) a.user_logits[t * E + ee] = l;
-        }
-      }
-      __syncthreads();
     }
+    // a fixed butterfly inside each warp, then the eight warps in order, then the bias
+#pragma unroll
+    for (int t = 0; t < kDecMaxT; ++t) {
+      float v = acc[t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0 && t < T) sh.red[warp][t] = v;
+    }
+    __syncthreads();
+    if (tid < T) {
+      float l = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kDecThreads / 32; ++w) l += sh.red[w][tid];
+      l += a.bias ? a.bias[e] : 0.0f;
+      a.logits[tid * E + e] = l;
+      if (a.user_logits) a.user_logits[tid * E + e] = l;
+    }
+    __syncthreads();
   }
   if (!dec_grid_sync(a, sh, 1)) return;
 
   // ---------------------------------------------------------------- top-k and slots
   {
+    // warp w takes tokens w, w + 8, ...: lane l holds the logits of experts l, l + 32, ...
+    // as order-preserving keys (NaN reads as -inf, -0 as +0); each of k rounds takes the largest
+    // key still free, ties to the lower expert index, with two warp reductions
     for (int t = warp; t < T; t += kDecThreads / 32) {
       float v[kDecMaxE / 32];
-      uint32_t taken = 0;
+      uint32_t key[kDecMaxE / 32];
 #pragma unroll
       for (int i = 0; i < kDecMaxE / 32; ++i) {
         const int e = lane + 32 * i;
-        if (e < E) {
-          const float l = a.logits[t * E + e];
-          v[i] = (l != l) ? -INFINITY : l;
-        } else {
-          v[i] = -INFINITY;
-          taken |= 1u << i;
-        }
+        v[i] = e < E ? __ldcg(a.logits + t * E + e) : -INFINITY;
       }
-      float lmax = 0.0f, sum = 0.0f, my_w = 0.0f;
+      uint32_t free_mask = 0;
+#pragma unroll
+      for (int i = 0; i < kDecMaxE / 32; ++i) {
+        float l = v[i];
+        if (l != l) l = -INFINITY;
+        if (l == 0.0f) l = 0.0f;  // -0 ties with +0
+        v[i] = l;
+        const uint32_t b = __float_as_uint(l);
+        key[i] = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+        if (lane + 32 * i < E) free_mask |= 1u << i;
+      }
+      float lmax = 0.0f, sum = 0.0f, my_v = 0.0f;
       int my_e = 0;
-      for (int j = 0; j < k; ++j) {  // lane j keeps slot j (ties to the lower expert index)
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
+      for (int j = 0; j < k; ++j) {
+        uint32_t bk = 0;
+        int bi = -1;
 #pragma unroll
-        for (int i = 0; i < kDecMaxE / 32; ++i) {
-          if (!((taken >> i) & 1u) && (be == 0x7fffffff || v[i] > bv)) {
-            bv = v[i];
-            be = lane + 32 * i;
+        for (int i = 0; i < kDecMaxE / 32; ++i)  // ascending i: a tie keeps the lower expert
+          if (((free_mask >> i) & 1u) && (bi < 0 || key[i] > bk)) {
+            bk = key[i];
+            bi = i;
           }
-        }
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
+        const int cand = (bi >= 0 && bk == kmax) ? lane + 32 * bi : 0x7fffffff;
+        const int we = (int)__reduce_min_sync(0xffffffffu, (unsigned)cand);
+        float wv = 0.0f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-          if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
-            bv = ov;
-            be = oe;
-          }
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        if (j == 0) lmax = bv;
-        const float ex = expf(bv - lmax);
-        sum += ex;
+        for (int i = 0; i < kDecMaxE / 32; ++i)
+          if (lane + 32 * i == we) wv = v[i];
+        wv = __shfl_sync(0xffffffffu, wv, we & 31);
+        if ((we & 31) == lane) free_mask &= ~(1u << (we >> 5));
+        if (j == 0) lmax = wv;
+        sum += expf(wv - lmax);
         if (lane == j) {
-          my_e = be;
-          my_w = ex;
+          my_e = we;
+          my_v = wv;
         }
       }
       if (lane < k) {
-        const float wt = my_w * (1.0f / sum);
+        const float wt = expf(my_v - lmax) * (1.0f / sum);
         sh.s_idx[t * k + lane] = my_e;
         sh.s_w[t * k + lane] = wt;
         if (blockIdx.x == 0) {
@@ -413,130 +388,250 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   auto slot_tok = [&](int s) { return s < P ? sh.slot_pair[s] / k : s - P; };
   const int KC1 = (H + kDecStepRows - 1) / kDecStepRows;  // 256-row steps of H
 
-  // ---------------------------------------------------------------- G: h = silu(x Wg) * (x Wu)
+  Ring ring;
+  ring.next_issue = ring.next_use = ring.inflight = 0;
+#pragma unroll
+  for (int b = 0; b < kDecBufs; ++b) ring.phase[b] = 0;
+  auto slot_rows = [&](int u, int& s0, int& ns) {
+    s0 = sh.ex_first[u];
+    ns = sh.ex_first[u + 1] - s0;
+  };
+
+  // ---------------------------------------------------------------- G: x Wg, x Wu per 256-row chunk
+  // Steps (expert u, chunk kc of H, 64-column block fb of F_u, gate|up) in that order, an
+  // even share of them per CTA: at any moment the CTAs stream neighbouring column blocks
+  // of the same weight rows. Each step's 16 x 64 product (a 256-row partial sum) is
+  // stored in part_g; phase H adds the chunks.
   {
-    // unit i -> (expert u, 64-column block fb of F_u); steps (kc, gate|up) over H
-    const int nfb_r = F / 64;
-    auto unit_of = [&](int i, int& u, int& fb) {
-      if (i < n_routed * nfb_r) {
-        u = i / nfb_r;
-        fb = i % nfb_r;
+    const int nfb_r = F / 64, nfb_s = Fs / 64;
+    auto nfb = [&](int u) { return u < n_routed ? nfb_r : nfb_s; };
+    const int64_t per_r = (int64_t)KC1 * nfb_r * 2;
+    const int64_t total = (int64_t)n_routed * per_r + (Fs > 0 ? (int64_t)KC1 * nfb_s * 2 : 0);
+    const int64_t s0 = total * blockIdx.x / G, s1 = total * (blockIdx.x + 1) / G;
+    struct Cur {
+      int u, kc, fb, gu;
+    };
+    auto at = [&](int64_t g) {
+      Cur c;
+      int64_t rem;
+      if (g < (int64_t)n_routed * per_r) {
+        c.u = (int)(g / per_r);
+        rem = g - (int64_t)c.u * per_r;
       } else {
-        u = n_routed;
-        fb = i - n_routed * nfb_r;
+        c.u = n_routed;
+        rem = g - (int64_t)n_routed * per_r;
+      }
+      const int nf2 = nfb(c.u) * 2;
+      c.kc = (int)(rem / nf2);
+      const int r2 = (int)(rem - (int64_t)c.kc * nf2);
+      c.fb = r2 >> 1;
+      c.gu = r2 & 1;
+      return c;
+    };
+    auto advance = [&](Cur& c) {
+      if (++c.gu == 2) {
+        c.gu = 0;
+        if (++c.fb == nfb(c.u)) {
+          c.fb = 0;
+          if (++c.kc == KC1) {
+            c.kc = 0;
+            ++c.u;
+          }
+        }
       }
     };
-    const int nunits = n_routed * nfb_r + (Fs > 0 ? Fs / 64 : 0);
-    auto nsteps = [&](int) { return 2 * KC1; };
-    auto step_info = [&](int i, int s, const CUtensorMap*& map, int& row0, int& col0, int& nrows) {
-      int u, fb;
-      unit_of(i, u, fb);
-      const int kc = s >> 1, up = s & 1, k0 = kc * kDecStepRows;
-      nrows = min(kDecStepRows, H - k0);
-      col0 = fb * 64;
-      if (u < n_routed) {
-        map = up ? &tm_up : &tm_gate;
-        row0 = sh.ex_id[u] * H + k0;
-      } else {
-        map = up ? &tm_sup : &tm_sgate;
-        row0 = k0;
-      }
+    auto issue = [&](const Cur& c) {
+      const int k0 = c.kc * kDecStepRows, nrows = min(kDecStepRows, H - k0);
+      if (c.u < n_routed)
+        ring_issue(sh, tiles, ring, c.gu ? &tm_up : &tm_gate, sh.ex_id[c.u] * H + k0, c.fb * 64, nrows);
+      else
+        ring_issue(sh, tiles, ring, c.gu ? &tm_sup : &tm_sgate, k0, c.fb * 64, nrows);
     };
-    auto needs_a = [&](int, int s) { return (s & 1) == 0; };
-    auto load_a = [&](int i, int s, uint4 (&v)[2]) {  // x rows of the unit's tokens, the step's 256 columns
-      int u, fb;
-      unit_of(i, u, fb);
-      const int k0 = (s >> 1) * kDecStepRows, nk = min(kDecStepRows, H - k0);
-      const int s0 = sh.ex_first[u], ns = sh.ex_first[u + 1] - s0;
+    // x rows of expert u's tokens, the 256 columns of chunk kc
+    auto load_a = [&](int u, int kc, uint4 (&v)[2]) {
+      const int k0 = kc * kDecStepRows, nk = min(kDecStepRows, H - k0);
+      int sb, ns;
+      slot_rows(u, sb, ns);
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const int idx = tid + q * kDecThreads, r = idx >> 5, c = idx & 31;
         v[q] = make_uint4(0, 0, 0, 0);
-        if (r < ns && c * 8 < nk) v[q] = *reinterpret_cast<const uint4*>(a.x + (int64_t)slot_tok(s0 + r) * H + k0 + c * 8);
+        if (r < ns && c * 8 < nk) v[q] = *reinterpret_cast<const uint4*>(a.x + (int64_t)slot_tok(sb + r) * H + k0 + c * 8);
       }
     };
-    auto store_a = [&](const uint4 (&v)[2]) {
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int idx = tid + q * kDecThreads, r = idx >> 5, c = idx & 31;
-        *reinterpret_cast<uint4*>(sh.a_tile + r * kDecALd + c * 8) = v[q];
+    if (s0 < s1) {
+      Cur ic = at(s0);
+      int64_t left = s1 - s0;
+      for (; ring.inflight < kDecBufs && left > 0; --left, advance(ic)) issue(ic);
+      Cur cc = at(s0);
+      // the A tile after the current one: (u, kc + 1), else (u + 1, 0), if this CTA reaches it
+      int nu = cc.u, nkc = cc.kc;
+      int64_t ng = s0 - (int64_t)((cc.fb * 2) + cc.gu);  // first step of the current A tile
+      uint4 av[2];
+      load_a(cc.u, cc.kc, av);
+      for (int64_t g = s0; g < s1; ++g, advance(cc)) {
+        if (g == s0 || (cc.fb == 0 && cc.gu == 0)) {
+          a_store(sh, av);  // the previous readers of the A tile passed the last barrier
+          ng += nfb(nu) * 2;
+          if (++nkc == KC1) {
+            nkc = 0;
+            ++nu;
+          }
+          if (ng < s1) load_a(nu, nkc, av);
+        }
+        uint32_t wt;
+        if (!ring_wait(sh, tiles, ring, a, wt)) return;
+        const int nrows = min(kDecStepRows, H - cc.kc * kDecStepRows);
+        float d0[4] = {0, 0, 0, 0}, d1[4] = {0, 0, 0, 0};
+        step_mma(sh, wt, nrows, d0, d1);
+        int sb, ns;
+        slot_rows(cc.u, sb, ns);
+        const int col = cc.fb * 64 + warp * 8 + (lane & 3) * 2, r0 = lane >> 2;
+        float* pg = a.part_g + ((int64_t)cc.kc * a.smax * 2 + cc.gu) * Fm + col;
+        if (r0 < ns)
+          *reinterpret_cast<float2*>(pg + (int64_t)(sb + r0) * 2 * Fm) = make_float2(d0[0] + d1[0], d0[1] + d1[1]);
+        if (r0 + 8 < ns)
+          *reinterpret_cast<float2*>(pg + (int64_t)(sb + r0 + 8) * 2 * Fm) =
+              make_float2(d0[2] + d1[2], d0[3] + d1[3]);
+        __syncthreads();  // this buffer (and, at an A step, the A tile) is free again
+        ring_release(ring);
+        if (left > 0) {
+          issue(ic);
+          advance(ic);
+          --left;
+        }
       }
-    };
-    float dg[4] = {0, 0, 0, 0}, du[4] = {0, 0, 0, 0};
-    auto mma = [&](int, int s, uint32_t wt, int nrows) {
-      if (s & 1) step_mma(sh, wt, nrows, du);
-      else step_mma(sh, wt, nrows, dg);
-    };
-    auto done = [&](int i) {
-      int u, fb;
-      unit_of(i, u, fb);
-      const int s0 = sh.ex_first[u], ns = sh.ex_first[u + 1] - s0;
-      const int col = fb * 64 + warp * 8 + (lane & 3) * 2, r0 = lane >> 2;
-      float h[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) h[q] = dg[q] * sigmoidf_(dg[q]) * du[q];
-      if (r0 < ns)
-        *reinterpret_cast<__nv_bfloat162*>(a.hbuf + (int64_t)(s0 + r0) * Fm + col) = __floats2bfloat162_rn(h[0], h[1]);
-      if (r0 + 8 < ns)
-        *reinterpret_cast<__nv_bfloat162*>(a.hbuf + (int64_t)(s0 + r0 + 8) * Fm + col) =
-            __floats2bfloat162_rn(h[2], h[3]);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dg[q] = du[q] = 0.0f;
-    };
-    if (!stream_steps(sh, tiles, bar_phase, nunits, a, nsteps, step_info, needs_a, load_a, store_a, mma, done)) return;
+    }
   }
-  if (!dec_grid_sync(a, sh, 2)) return;
+
+  // ---------------------------------------------------------------- D: y = h Wd (its first copies)
+  // Units (expert u, 64 columns hb of H), CTA b taking units b, b + G, ...; each streams
+  // all F_u rows of W_down in 256-row steps. The first tiles are issued now, before the
+  // barriers, so they land while phase H runs.
+  const int nhb = H / 64;
+  const int nunits_d = n_u * nhb;
+  const int mine_d = nunits_d > (int)blockIdx.x ? (nunits_d - (int)blockIdx.x + G - 1) / G : 0;
+  auto fu = [&](int u) { return u < n_routed ? F : Fs; };
+  auto kc2 = [&](int u) { return (fu(u) + kDecStepRows - 1) / kDecStepRows; };
+  struct DCur {
+    int li, fk;
+  };
+  auto d_unit = [&](const DCur& c) { return (int)blockIdx.x + c.li * G; };
+  auto d_advance = [&](DCur& c) {
+    if (++c.fk == kc2(d_unit(c) / nhb)) {
+      c.fk = 0;
+      ++c.li;
+    }
+  };
+  auto d_issue = [&](const DCur& c) {
+    const int i = d_unit(c), u = i / nhb, hb = i % nhb, k0 = c.fk * kDecStepRows;
+    const int nrows = min(kDecStepRows, fu(u) - k0);
+    if (u < n_routed)
+      ring_issue(sh, tiles, ring, &tm_down, sh.ex_id[u] * F + k0, hb * 64, nrows);
+    else
+      ring_issue(sh, tiles, ring, &tm_sdown, k0, hb * 64, nrows);
+  };
+  DCur dic{0, 0};
+  dec_grid_arrive(a, sh);
+  for (; ring.inflight < kDecBufs && dic.li < mine_d; d_advance(dic)) d_issue(dic);
+  if (!dec_grid_wait(a, sh, 2)) {
+    if (tid == 0)  // let the copies already issued land before the shared memory is released
+      for (int q = 0; q < ring.inflight; ++q) {
+        const int bq = (ring.next_use + q) % kDecBufs;
+        mbar_wait_timed(&sh.bar[bq], ring.phase[bq], 200000000ull);
+      }
+    __syncthreads();
+    return;
+  }
+
+  // ---------------------------------------------------------------- H: h = silu(sum_kc g) * (sum_kc u)
+  {
+    const int S = n_routed > 0 ? sh.ex_first[n_u] : 0;
+    const int f8 = Fm / 8;
+    // item idx -> CTA idx % G, so that a few items still use many SMs
+    for (int idx = (int)blockIdx.x + G * tid; idx < S * f8; idx += G * kDecThreads) {
+      const int sl = idx / f8, f = (idx - sl * f8) * 8;
+      if (f >= (sl < P ? F : Fs)) continue;
+      float gs[8], us[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) gs[q] = us[q] = 0.0f;
+#pragma unroll 8
+      for (int kc = 0; kc < KC1; ++kc) {  // chunks in order
+        const float* pg = a.part_g + (((int64_t)kc * a.smax + sl) * 2) * Fm + f;
+        const float4 g0 = __ldcg(reinterpret_cast<const float4*>(pg));
+        const float4 g1 = __ldcg(reinterpret_cast<const float4*>(pg + 4));
+        const float4 u0 = __ldcg(reinterpret_cast<const float4*>(pg + Fm));
+        const float4 u1 = __ldcg(reinterpret_cast<const float4*>(pg + Fm + 4));
+        gs[0] += g0.x; gs[1] += g0.y; gs[2] += g0.z; gs[3] += g0.w;
+        gs[4] += g1.x; gs[5] += g1.y; gs[6] += g1.z; gs[7] += g1.w;
+        us[0] += u0.x; us[1] += u0.y; us[2] += u0.z; us[3] += u0.w;
+        us[4] += u1.x; us[5] += u1.y; us[6] += u1.z; us[7] += u1.w;
+      }
+      float h[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) h[q] = gs[q] * sigmoidf_(gs[q]) * us[q];
+      *reinterpret_cast<uint4*>(a.hbuf + (int64_t)sl * Fm + f) = f_to_bf16x8(h);
+    }
+  }
+  if (!dec_grid_sync(a, sh, 3)) {
+    if (tid == 0)
+      for (int q = 0; q < ring.inflight; ++q) {
+        const int bq = (ring.next_use + q) % kDecBufs;
+        mbar_wait_timed(&sh.bar[bq], ring.phase[bq], 200000000ull);
+      }
+    __syncthreads();
+    return;
+  }
 
   // ---------------------------------------------------------------- D: y = h Wd
   {
-    const int nhb = H / 64;
-    const int nunits = n_u * nhb;
-    auto fu = [&](int u) { return u < n_routed ? F : Fs; };
-    auto nsteps = [&](int i) { return (fu(i / nhb) + kDecStepRows - 1) / kDecStepRows; };
-    auto step_info = [&](int i, int s, const CUtensorMap*& map, int& row0, int& col0, int& nrows) {
-      const int u = i / nhb, hb = i % nhb, k0 = s * kDecStepRows;
-      nrows = min(kDecStepRows, fu(u) - k0);
-      col0 = hb * 64;
-      if (u < n_routed) {
-        map = &tm_down;
-        row0 = sh.ex_id[u] * F + k0;
-      } else {
-        map = &tm_sdown;
-        row0 = k0;
-      }
-    };
-    auto needs_a = [&](int, int) { return true; };
-    auto load_a = [&](int i, int s, uint4 (&v)[2]) {  // h rows of the unit's slots, the step's 256 columns
-      const int u = i / nhb, k0 = s * kDecStepRows, nk = min(kDecStepRows, fu(u) - k0);
-      const int s0 = sh.ex_first[u], ns = sh.ex_first[u + 1] - s0;
+    // h rows of unit i's slots, the 256 columns of step fk
+    auto load_a = [&](const DCur& c, uint4 (&v)[2]) {
+      const int u = d_unit(c) / nhb, k0 = c.fk * kDecStepRows, nk = min(kDecStepRows, fu(u) - k0);
+      int sb, ns;
+      slot_rows(u, sb, ns);
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        const int idx = tid + q * kDecThreads, r = idx >> 5, c = idx & 31;
+        const int idx = tid + q * kDecThreads, r = idx >> 5, c8 = idx & 31;
         v[q] = make_uint4(0, 0, 0, 0);
-        if (r < ns && c * 8 < nk) v[q] = *reinterpret_cast<const uint4*>(a.hbuf + (int64_t)(s0 + r) * Fm + k0 + c * 8);
+        if (r < ns && c8 * 8 < nk)
+          v[q] = __ldcg(reinterpret_cast<const uint4*>(a.hbuf + (int64_t)(sb + r) * Fm + k0 + c8 * 8));
       }
     };
-    auto store_a = [&](const uint4 (&v)[2]) {
+    float d0[4] = {0, 0, 0, 0}, d1[4] = {0, 0, 0, 0};
+    uint4 av[2];
+    DCur cc{0, 0}, ac{0, 0};
+    if (mine_d > 0) load_a(ac, av);
+    for (; cc.li < mine_d; d_advance(cc)) {
+      a_store(sh, av);  // every step starts an A tile; its previous readers passed the last barrier
+      d_advance(ac);
+      if (ac.li < mine_d) load_a(ac, av);
+      uint32_t wt;
+      if (!ring_wait(sh, tiles, ring, a, wt)) return;
+      const int i = d_unit(cc), u = i / nhb;
+      step_mma(sh, wt, min(kDecStepRows, fu(u) - cc.fk * kDecStepRows), d0, d1);
+      if (cc.fk + 1 == kc2(u)) {  // the unit's last step: its y rows
+        const int hb = i % nhb;
+        int sb, ns;
+        slot_rows(u, sb, ns);
+        const int col = hb * 64 + warp * 8 + (lane & 3) * 2, r0 = lane >> 2;
+        if (r0 < ns)
+          *reinterpret_cast<float2*>(a.ypair + (int64_t)(sb + r0) * H + col) = make_float2(d0[0] + d1[0], d0[1] + d1[1]);
+        if (r0 + 8 < ns)
+          *reinterpret_cast<float2*>(a.ypair + (int64_t)(sb + r0 + 8) * H + col) =
+              make_float2(d0[2] + d1[2], d0[3] + d1[3]);
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int idx = tid + q * kDecThreads, r = idx >> 5, c = idx & 31;
-        *reinterpret_cast<uint4*>(sh.a_tile + r * kDecALd + c * 8) = v[q];
+        for (int q = 0; q < 4; ++q) d0[q] = d1[q] = 0.0f;
       }
-    };
-    float d[4] = {0, 0, 0, 0};
-    auto mma = [&](int, int, uint32_t wt, int nrows) { step_mma(sh, wt, nrows, d); };
-    auto done = [&](int i) {
-      const int u = i / nhb, hb = i % nhb;
-      const int s0 = sh.ex_first[u], ns = sh.ex_first[u + 1] - s0;
-      const int col = hb * 64 + warp * 8 + (lane & 3) * 2, r0 = lane >> 2;
-      if (r0 < ns) *reinterpret_cast<float2*>(a.ypair + (int64_t)(s0 + r0) * H + col) = make_float2(d[0], d[1]);
-      if (r0 + 8 < ns) *reinterpret_cast<float2*>(a.ypair + (int64_t)(s0 + r0 + 8) * H + col) = make_float2(d[2], d[3]);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) d[q] = 0.0f;
-    };
-    if (!stream_steps(sh, tiles, bar_phase, nunits, a, nsteps, step_info, needs_a, load_a, store_a, mma, done)) return;
+      __syncthreads();  // this buffer and the A tile are free again
+      ring_release(ring);
+      if (dic.li < mine_d) {
+        d_issue(dic);
+        d_advance(dic);
+      }
+    }
   }
-  if (!dec_grid_sync(a, sh, 3)) return;
+  if (!dec_grid_sync(a, sh, 4)) return;
 
   // ---------------------------------------------------------------- C: combine
   for (int idx = blockIdx.x * kDecThreads + tid; idx < T * (H / 4); idx += G * kDecThreads) {
@@ -544,7 +639,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     float4 v[kDecMaxK];
 #pragma unroll
     for (int j = 0; j < kDecMaxK; ++j)  // every slot's row loaded before the sum
-      if (j < k) v[j] = *reinterpret_cast<const float4*>(a.ypair + (int64_t)sh.slot_of_pair[t * k + j] * H + c);
+      if (j < k) v[j] = __ldcg(reinterpret_cast<const float4*>(a.ypair + (int64_t)sh.slot_of_pair[t * k + j] * H + c));
     float acc[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int j = 0; j < kDecMaxK; ++j) {  // slots j ascending, then the shared expert
@@ -557,7 +652,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
     }
     if (Fs > 0) {
-      const float4 sv = *reinterpret_cast<const float4*>(a.ypair + (int64_t)(P + t) * H + c);
+      const float4 sv = __ldcg(reinterpret_cast<const float4*>(a.ypair + (int64_t)(P + t) * H + c));
       acc[0] += sv.x;
       acc[1] += sv.y;
       acc[2] += sv.z;
@@ -596,10 +691,13 @@ static bool dec_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols)
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t decode_scratch_bytes(int64_t T, int64_t H, int64_t F, int64_t E, int64_t Fs) {
-  const int64_t Fm = F > Fs ? F : Fs;
+// rows of the slot-indexed buffers: the T * k routed pairs and T shared-expert tokens
+static int64_t dec_slots(int64_t T, int64_t k) { return T * k + T; }
+
+size_t decode_scratch_bytes(int64_t T, int64_t H, int64_t F, int64_t E, int64_t k, int64_t Fs) {
+  const int64_t Fm = F > Fs ? F : Fs, S = dec_slots(T, k), KC1 = (H + kDecStepRows - 1) / kDecStepRows;
   auto up = [](int64_t n) { return (size_t)((n + 255) / 256 * 256); };
-  return up(T * E * 4) + up((int64_t)kDecMaxSlots * Fm * 2) + up((int64_t)kDecMaxSlots * H * 4) + 256;
+  return up(T * E * 4) + up(S * Fm * 2) + up(S * H * 4) + up(KC1 * S * 2 * Fm * 4) + 256;
 }
 
 bool decode_supported(int64_t T, int64_t H, int64_t F, int64_t E, int64_t k, int64_t Fs) {
@@ -612,7 +710,7 @@ cudaError_t launch_decode_fwd(int T, int H, int F, int E, int k, int Fs, const v
                               const void* ws_gate, const void* ws_up, const void* ws_down, void* y, int* topk_idx,
                               float* topk_w, int* user_idx, float* user_w, float* user_logits, void* scratch,
                               int* status, int num_sms, cudaStream_t st) {
-  const int64_t Fm = F > Fs ? F : Fs;
+  const int64_t Fm = F > Fs ? F : Fs, S = dec_slots(T, k), KC1 = (H + kDecStepRows - 1) / kDecStepRows;
   auto up = [](int64_t n) { return (int64_t)((n + 255) / 256 * 256); };
   char* b = static_cast<char*>(scratch);
   DecodeArgs a;
@@ -629,9 +727,12 @@ cudaError_t launch_decode_fwd(int T, int H, int F, int E, int k, int Fs, const v
   a.logits = reinterpret_cast<float*>(b);
   b += up((int64_t)T * E * 4);
   a.hbuf = reinterpret_cast<__nv_bfloat16*>(b);
-  b += up((int64_t)kDecMaxSlots * Fm * 2);
+  b += up(S * Fm * 2);
   a.ypair = reinterpret_cast<float*>(b);
-  b += up((int64_t)kDecMaxSlots * H * 4);
+  b += up(S * H * 4);
+  a.part_g = reinterpret_cast<float*>(b);
+  a.smax = (int)S;
+  b += up(KC1 * S * 2 * Fm * 4);
   a.sync = reinterpret_cast<unsigned*>(b);
   a.status = status;
   cudaError_t e = cudaMemsetAsync(a.sync, 0, sizeof(unsigned), st);

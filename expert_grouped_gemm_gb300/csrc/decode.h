@@ -8,8 +8,9 @@ namespace moe {
 
 // dims the fused kernel handles: 1 <= T <= 16, E <= 256, k <= 16, H, F, Fs <= 4096 (multiples of 64)
 bool decode_supported(int64_t T, int64_t H, int64_t F, int64_t E, int64_t k, int64_t Fs);
-// bytes of device scratch it needs (router, gate/up and down partial sums, h, a barrier counter)
-size_t decode_scratch_bytes(int64_t T, int64_t H, int64_t F, int64_t E, int64_t Fs);
+// bytes of device scratch it needs (logits, h, per-slot y, gate/up partial sums per 256-row
+// chunk of H, a barrier counter)
+size_t decode_scratch_bytes(int64_t T, int64_t H, int64_t F, int64_t E, int64_t k, int64_t Fs);
 // one cooperative launch of num_sms CTAs on st
 cudaError_t launch_decode_fwd(int T, int H, int F, int E, int k, int Fs, const void* x, const void* w_router,
                               const float* bias, const void* w_gate, const void* w_up, const void* w_down,

@@ -123,7 +123,7 @@ WsLayout make_layout(const moe_dims* d) {
       L.part_elems * 4,                                // part
       (P / 256 + E + 1) * 16, (P / 256 + E + 1) * 16,  // tile_rec2 ret_tile_rec2
       (int64_t)(d->dtype == MOE_BF16 && decode_supported(T, H, F, E, k, Fs)  // decode scratch (T <= 16)
-                    ? decode_scratch_bytes(T, H, F, E, Fs)
+                    ? decode_scratch_bytes(T, H, F, E, k, Fs)
                     : 0),
   };
   L.n = (int)(sizeof(sizes) / sizeof(sizes[0]));

@@ -112,3 +112,18 @@ def test_decode_rejects_unsupported_dims():
     with pytest.raises(_lib.MoeError) as ei:
         layer.forward_decode(inp["x"].cuda())
     assert ei.value.code == _lib.MOE_ERR_UNSUPPORTED
+
+
+def test_decode_router_ties_go_to_the_lower_expert():
+    """A zero router leaves logits = bias exactly; bias values repeat every 5 experts, so
+    the top-8 is a tie among 26 experts at 0 and must take the lowest indices."""
+    w = custom("dec_ties", T=4, k=8, **QWEN)
+    inp = make_inputs(w, seed=9)
+    inp["w_router"] = torch.zeros_like(inp["w_router"])
+    inp["router_bias"] = -(torch.arange(w.E) % 5).to(torch.float32)
+    g, _ = run_decode(w, inp)
+    assert g["status"] == 0
+    want = np.tile(np.arange(0, 40, 5), (w.T, 1))
+    assert np.array_equal(g["idx"], want), g["idx"]
+    assert np.all(g["w"] == np.float32(0.125))
+    check_decode(w, inp, g)
