@@ -4,25 +4,32 @@
 // At a handful of tokens the layer is a weight stream: each token touches k experts,
 // and their W_gate, W_up, W_down dominate the bytes. The unfused path runs a dozen
 // short kernels whose launch, prologue and pipeline fill cost more than the stream.
-// Here one cooperative launch (one CTA per SM, every CTA resident) runs four phases
+// Here one cooperative launch (one CTA per SM, every CTA resident) runs these phases,
 // separated by grid-wide barriers:
 //   R  router logits: CTA b computes logits[t, b], logits[t, b + G], ... over all of H
 //      (CUDA cores), with the bias added;
-//   G  every CTA takes the top-k and the renormalised softmax weights of every token
+//   K  every CTA takes the top-k and the renormalised softmax weights of every token
 //      and builds the same slot table (the routed (token, expert) pairs sorted by
-//      expert then token, then one slot per token for the shared expert); then units
-//      (expert, 64 columns of F) stream all of H of W_gate and W_up through a ring of
-//      four 32 KB shared-memory tiles (TMA, 128-byte swizzle) and meet the expert's
-//      tokens in mma.sync m16n8k16 bf16 products with fp32 accumulation (gate and up in
-//      two accumulators), and write h = silu(a) * b in bf16;
-//   D  units (expert, 64 columns of H) stream all of F of W_down the same way and
-//      write y for the expert's slots in fp32;
+//      expert then token, then one slot per token for the shared expert);
+//   G  x W_gate and x W_up: units (expert, column block of at most 768 columns) whose
+//      steps are 32-row slices of H read end to end (a row block of the weight); each
+//      CTA takes an even share of all steps (K split) and adds a unit's steps in
+//      registers, storing the sums of a unit it streamed whole, or its piece of a
+//      split unit;
+//   H  h = silu(g) * u per slot, g and u the sums of each unit's pieces in CTA order;
+//   D  y = h W_down: units (expert, 64 columns of H) taken round-robin, each streaming
+//      all F_u rows in 256-row steps; its first copies are issued before phase H, so
+//      they land while it runs;
 //   C  y[t] = sum_j w_tj y(t, j) (+ the shared expert), slots in order, rounded once.
-// At most 16 tokens make the contractions 16 rows wide, so the weight stream, not the
-// tensor rate, bounds them; no K is split, so no partial sums are reduced between
-// phases. Every sum runs in a fixed order, so two calls give the same bits. Every wait
-// (TMA landing, grid barrier) is bounded: a wait that runs out sets MOE_ERR_TIMEOUT in
-// the status word and the kernel returns.
+// The weight steps move through a ring of four 48 KB shared-memory tiles (TMA, 128-byte
+// swizzle). One producer warp issues the copies as soon as a tile is free; eight
+// consumer warps multiply (mma.sync m16n8k16, bf16 in, fp32 accumulators; warp w owns
+// the 8-column n-tile w of every 64-column box) and free a tile as soon as each has
+// read it, so that a tile is refilled without waiting for the block. At most 16 tokens
+// make the contractions 16 rows wide: the weight stream, not the tensor rate, bounds
+// them. Every sum runs in a fixed order, so two calls give the same bits. Every wait
+// (TMA landing, a free tile, a grid barrier) is bounded: a wait that runs out sets
+// MOE_ERR_TIMEOUT in the status word and the kernel returns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -32,17 +39,28 @@
 
 namespace moe {
 
-constexpr int kDecMaxT = 16;      // tokens (the mma M dimension)
-constexpr int kDecThreads = 256;  // 8 warps: one 8-column n-tile of a 64-column unit each
-constexpr int kDecStepRows = 256; // weight rows per ring step: four 64-row boxes
-constexpr int kDecBufs = 6;       // weight tiles in flight per CTA
+constexpr int kDecMaxT = 16;                  // tokens (the mma M dimension)
+constexpr int kDecThreads = 256;              // consumer threads: 8 warps
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kDecBlock = kDecThreads + 32;   // + the producer warp
+constexpr int kDecBufs = 4;                   // ring tiles
+constexpr int kDecTileBytes = 49152;          // one ring tile: 48 KB
+// gate/up steps: 32 rows of H x up to 12 boxes of 64 columns side by side
+constexpr int kDecGRows = 32;
+constexpr int kDecGMaxBox = 12;
+constexpr int kDecGBoxBytes = kDecGRows * 128;  // 4 KB
+constexpr int kDecGMaxCols = kDecGMaxBox * 64;
+// down steps: 256 rows of F_u x 64 columns of H (four 64-row boxes, 32 KB), then the
+// step's A tile: the expert's h rows x the same 256 columns (four 16-row boxes, 8 KB)
+constexpr int kDecStepRows = 256;
 constexpr int kDecBoxRows = 64;
-constexpr int kDecTileBytes = kDecStepRows * 128;            // 32 KB: 256 rows x 64 bf16
-constexpr int kDecALd = kDecStepRows + 8;                    // A tile row stride (elements), padded
+constexpr int kDecDABoxRows = 16;
+constexpr int kDecDAOffset = 32768;
 constexpr int kDecMaxE = 256;
 constexpr int kDecMaxK = 16;  // T * k <= 256: one thread per routed pair when ranking them
 constexpr int kDecMaxH = 4096;
-constexpr uint64_t kDecWaitNs = 1000000000ull;                // 1 s
+constexpr int kDecMaxGrid = 256;  // CTAs of one launch at most (one per SM)
+constexpr uint64_t kDecWaitNs = 1000000000ull;  // 1 s
 
 struct DecodeArgs {
   int T, H, F, E, k, Fs;
@@ -58,29 +76,37 @@ struct DecodeArgs {
   float* logits;      // [T][E] biased fp32 logits
   __nv_bfloat16* hbuf;  // [slots][Fm]
   float* ypair;       // [slots][H]
-  float* part_g;      // [H / 256][slots][gate, up][Fm]: x Wg and x Wu over one 256-row chunk of H
-  int smax;           // slot rows of part_g: T * k + T
+  float* part_g;      // [slots][gate, up][Fm]: x Wg and x Wu of a unit streamed by one CTA
+  float* piece_g;     // [2 * kDecMaxGrid][gate, up][T][kDecGMaxCols]: pieces of split units
   unsigned* sync;     // grid barrier counter (zeroed before the launch)
   int* status;
 };
 
 struct DecodeShared {
-  __nv_bfloat16 a_tile[kDecMaxT * kDecALd];  // tokens x rows of the current step
-  float red[kDecThreads / 32][kDecMaxT];     // router: one partial sum per warp and token
+  float red[kDecWarps][kDecMaxT];            // router: one partial sum per warp and token
   int s_idx[kDecMaxT * kDecMaxK];
   float s_w[kDecMaxT * kDecMaxK];
   int slot_pair[kDecMaxT * kDecMaxK];        // routed slot -> pair t*k + j
   int slot_of_pair[kDecMaxT * kDecMaxK];
   int ex_id[kDecMaxT * kDecMaxK + 1];        // unit expert u -> expert id (shared: -1)
   int ex_first[kDecMaxT * kDecMaxK + 2];     // first slot of expert u; ex_first[n_u] = slots
-  uint64_t bar[kDecBufs];
+  int slot_u[kDecMaxT * kDecMaxK + kDecMaxT];  // slot -> unit expert u
+  int cta_start[kDecMaxGrid + 1];            // first gate/up step of every CTA
+  uint64_t full[kDecBufs];                   // a tile's copies landed
+  uint64_t empty[kDecBufs];                  // every consumer warp has read the tile
   int n_routed, n_u;
+  int h_ready;                               // phase H is done grid-wide: down A tiles may be copied
   int abort_flag;
 };
 
 // ------------------------------------------------------------------ small helpers
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
@@ -101,16 +127,46 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// barrier of the eight consumer warps only (the producer warp runs its own loop)
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kDecThreads) : "memory"); }
+// tx bytes expected on a barrier, without an arrival
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
 
 // Grid-wide barrier number `phase` (1, 2, ...), in two halves so that a CTA can issue
 // work between them: arrive (every CTA once: a release add after the CTA's own barrier)
-// and wait (thread 0 polls with acquire loads). wait returns false when the wait ran
-// out (or an earlier one did), after recording MOE_ERR_TIMEOUT.
+// and wait (thread 0 polls with acquire loads). The CTA's own barrier covers all threads
+// (kAll) before the producer warp starts its loop, the consumer warps after. wait
+// returns false when the wait ran out (or an earlier one did), after recording
+// MOE_ERR_TIMEOUT.
+template <bool kAll>
+__device__ __forceinline__ void block_sync() {
+  if (kAll)
+    __syncthreads();
+  else
+    consumer_sync();
+}
+// the same barrier, returning whether any participating thread passed true: every
+// thread leaves with the same answer, even when another warp changes the flag it read
+template <bool kAll>
+__device__ __forceinline__ bool block_any(bool p) {
+  if (kAll) return __syncthreads_or(p) != 0;
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q, o;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred o, 1, %2, q;\n\tselp.u32 %0, 1, 0, o;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)p), "n"(kDecThreads)
+      : "memory");
+  return r != 0;
+}
+template <bool kAll>
 __device__ __forceinline__ void dec_grid_arrive(const DecodeArgs& a, DecodeShared& sh) {
-  __syncthreads();
+  block_sync<kAll>();
   if (threadIdx.x == 0 && !sh.abort_flag)
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a.sync), "r"(1u) : "memory");
 }
+template <bool kAll>
 __device__ bool dec_grid_wait(const DecodeArgs& a, DecodeShared& sh, unsigned phase) {
   if (threadIdx.x == 0 && !sh.abort_flag) {
     const unsigned target = phase * gridDim.x;
@@ -125,174 +181,166 @@ __device__ bool dec_grid_wait(const DecodeArgs& a, DecodeShared& sh, unsigned ph
       }
     }
   }
-  __syncthreads();
-  return !sh.abort_flag;
-}
-__device__ __forceinline__ bool dec_grid_sync(const DecodeArgs& a, DecodeShared& sh, unsigned phase) {
-  dec_grid_arrive(a, sh);
-  return dec_grid_wait(a, sh, phase);
+  return !block_any<kAll>(*(volatile int*)&sh.abort_flag != 0);
 }
 
-// d0 + d1 += (sh.a_tile, nrows columns) x (weight tile at wt, nrows rows x 64 columns):
-// warp w takes the 16 x 8 block of columns 8w .. 8w+7 (rows = tokens). Even 16-row
-// slices go to d0, odd ones to d1, so two mma chains are in flight; nrows is a multiple
-// of 64.
-__device__ __forceinline__ void step_mma(const DecodeShared& sh, uint32_t wt, int nrows, float (&d0)[4],
-                                         float (&d1)[4]) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t a_base = smem_u32(sh.a_tile);
-#pragma unroll 2
-  for (int kk = 0; kk < nrows; kk += 32) {
-    uint32_t a0, a1, a2, a3, b0, b1, c0, c1, c2, c3, e0, e1;
-    // A: matrices (rows 0-7, k 0-7), (8-15, 0-7), (0-7, 8-15), (8-15, 8-15)
-    const int ar = lane & 15, ak = kk + ((lane >> 4) << 3);
-    ldsm_x4(a_base + (uint32_t)((ar * kDecALd + ak) * 2), a0, a1, a2, a3);
-    ldsm_x4(a_base + (uint32_t)((ar * kDecALd + ak + 16) * 2), c0, c1, c2, c3);
-    // B: weight rows kk..kk+15, columns 8w..8w+7 (16-byte chunk w of each swizzled row)
-    const int br = kk + (lane & 15), br2 = br + 16;
-    ldsm_x2_trans(wt + (uint32_t)(br * 128 + ((warp ^ (br & 7)) << 4)), b0, b1);
-    ldsm_x2_trans(wt + (uint32_t)(br2 * 128 + ((warp ^ (br2 & 7)) << 4)), e0, e1);
-    mma_16816(d0, a0, a1, a2, a3, b0, b1);
-    mma_16816(d1, c0, c1, c2, c3, e0, e1);
-  }
-}
-
-// The weight ring: kDecBufs shared-memory tiles of at most 256 rows x 64 columns, filled
-// by TMA in issue order and consumed in the same order. Every thread keeps the same copy
-// of this state; thread 0 issues the copies.
-struct Ring {
-  int next_issue, next_use, inflight;
-  uint32_t phase[kDecBufs];
+// The steps of the gate/up phase; CTA c takes the steps [start(c), start(c + 1)), an
+// even share, so a unit may be split between neighbouring CTAs (K split).
+struct PhaseSteps {
+  int64_t total;
+  int G;
+  __device__ int64_t start(int c) const { return total * c / G; }
+  __device__ int cta_of(int64_t g) const { return (int)(((g + 1) * G - 1) / total); }  // last c with start(c) <= g
+};
+// The same in 32-bit arithmetic with the starts tabled (total * G < 2^31): for the
+// reduce phase, which asks it for every item.
+struct PhaseTable {
+  const int* start;  // start[c], c <= G
+  uint32_t total, G;
+  __device__ int cta_of(uint32_t g) const { return (int)(((g + 1) * G - 1) / total); }
 };
 
-__device__ __forceinline__ void ring_issue(DecodeShared& sh, uint8_t* tiles, Ring& r, const CUtensorMap* map,
-                                           int row0, int col0, int nrows) {
-  const int b = r.next_issue;
-  r.next_issue = (b + 1) % kDecBufs;
-  ++r.inflight;
-  if (threadIdx.x == 0) {
-    const int nbox = (nrows + kDecBoxRows - 1) / kDecBoxRows;
-    fence_async_smem();  // this CTA's earlier reads of the buffer come before the copy
-    mbar_arrive_expect_tx(&sh.bar[b], (uint32_t)(nbox * kDecBoxRows * 128));
-    for (int x = 0; x < nbox; ++x)
-      tma_load_2d(smem_u32(tiles + b * kDecTileBytes + x * kDecBoxRows * 128), map, smem_u32(&sh.bar[b]), col0,
-                  row0 + x * kDecBoxRows);
-  }
+// Consumer wait for ring tile j (sequence number): its copies landed. False after the
+// wait ran out or another role gave up.
+__device__ __forceinline__ bool wait_full(DecodeShared& sh, const DecodeArgs& a, int j) {
+  const int b = j % kDecBufs;
+  if (mbar_wait_bounded(&sh.full[b], (uint32_t)((j / kDecBufs) & 1), (volatile int*)&sh.abort_flag, kDecWaitNs))
+    return true;
+  set_status(a.status, MOE_ERR_TIMEOUT);
+  return false;
+}
+// Consumer warp done with tile j.
+__device__ __forceinline__ void release(DecodeShared& sh, int j) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.empty[j % kDecBufs]);
 }
 
-// Waits for the oldest tile in flight and returns its shared-memory address in wt; false
-// after a wait ran out, once this CTA's other copies in flight have landed (so that its
-// shared memory may be released).
-__device__ __forceinline__ bool ring_wait(DecodeShared& sh, uint8_t* tiles, Ring& r, const DecodeArgs& a,
-                                          uint32_t& wt) {
-  const int b = r.next_use;
-  const bool landed = mbar_wait_bounded(&sh.bar[b], r.phase[b], (volatile int*)&sh.abort_flag, kDecWaitNs);
-  if (landed)
-    r.phase[b] ^= 1u;
-  else
-    set_status(a.status, MOE_ERR_TIMEOUT);
-  __syncthreads();
-  if (sh.abort_flag) {
-    if (threadIdx.x == 0)
-      for (int q = landed ? 1 : 0; q < r.inflight; ++q) {
-        const int bq = (b + q) % kDecBufs;
-        mbar_wait_timed(&sh.bar[bq], r.phase[bq], 200000000ull);
-      }
-    __syncthreads();
-    return false;
-  }
-  wt = smem_u32(tiles + b * kDecTileBytes);
-  return true;
-}
-
-// After the barrier that ends the step: the oldest tile's buffer is free again.
-__device__ __forceinline__ void ring_release(Ring& r) {
-  r.next_use = (r.next_use + 1) % kDecBufs;
-  --r.inflight;
-}
-
-// A tile of the current step: up to 16 rows (the unit's tokens) x 256 columns, two
-// 16-byte pieces per thread, staged in registers one tile ahead.
-__device__ __forceinline__ void a_store(DecodeShared& sh, const uint4 (&v)[2]) {
+// acc[x] += A (16 rows x 32 columns, fragments in registers) x (box x of the tile at wt:
+// 32 rows x 64 columns) for the nbx boxes of a gate/up step: warp w takes columns
+// 8w .. 8w+7 of every box, so its nbx accumulators are independent chains.
+__device__ __forceinline__ void step_mma_rows(uint32_t wt, int nbx, const uint32_t (&af)[2][4],
+                                              float (&acc)[kDecGMaxBox][4]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int idx = threadIdx.x + q * kDecThreads, r = idx >> 5, c = idx & 31;
-    *reinterpret_cast<uint4*>(sh.a_tile + r * kDecALd + c * 8) = v[q];
+  for (int kq = 0; kq < 2; ++kq) {
+    const int br = kq * 16 + (lane & 15);
+    const uint32_t boff = (uint32_t)(br * 128 + ((warp ^ (br & 7)) << 4));
+#pragma unroll
+    for (int x = 0; x < kDecGMaxBox; ++x) {
+      if (x < nbx) {
+        uint32_t b0, b1;
+        ldsm_x2_trans(wt + (uint32_t)(x * kDecGBoxBytes) + boff, b0, b1);
+        mma_16816(acc[x], af[kq][0], af[kq][1], af[kq][2], af[kq][3], b0, b1);
+      }
+    }
+  }
+}
+
+// d0 + d1 += (the step's A tile at wt + kDecDAOffset: 16 rows x nrows columns, four
+// swizzled 16-row boxes) x (the weight tile at wt: nrows rows x 64 columns): warp w
+// takes columns 8w .. 8w+7; even 16-row slices go to d0, odd ones to d1.
+__device__ __forceinline__ void step_mma_down(uint32_t wt, int nrows, float (&d0)[4], float (&d1)[4]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t at = wt + kDecDAOffset;
+  const int ar = lane & 15;
+#pragma unroll 2
+  for (int kk = 0; kk < nrows; kk += 32) {
+    uint32_t a[2][4], b[2][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int k0 = kk + 16 * h;
+      const int chunk = ((k0 & 63) >> 3) + (lane >> 4);  // 16-byte chunk of the A box row
+      ldsm_x4(at + (uint32_t)((k0 >> 6) * (kDecDABoxRows * 128) + ar * 128 + ((chunk ^ (ar & 7)) << 4)), a[h][0],
+              a[h][1], a[h][2], a[h][3]);
+      const int br = k0 + (lane & 15);
+      ldsm_x2_trans(wt + (uint32_t)(br * 128 + ((warp ^ (br & 7)) << 4)), b[h][0], b[h][1]);
+    }
+    mma_16816(d0, a[0][0], a[0][1], a[0][2], a[0][3], b[0][0], b[0][1]);
+    mma_16816(d1, a[1][0], a[1][1], a[1][2], a[1][3], b[1][0], b[1][1]);
   }
 }
 
 // ------------------------------------------------------------------ the kernel
-__global__ void __launch_bounds__(kDecThreads, 1)
+__global__ void __launch_bounds__(kDecBlock, 1)
     k_decode_fwd(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
                  const __grid_constant__ CUtensorMap tm_down, const __grid_constant__ CUtensorMap tm_sgate,
                  const __grid_constant__ CUtensorMap tm_sup, const __grid_constant__ CUtensorMap tm_sdown,
-                 const DecodeArgs a) {
+                 const __grid_constant__ CUtensorMap tm_h, const DecodeArgs a) {
   extern __shared__ uint8_t dec_smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dec_smem_raw) + 1023) & ~uintptr_t(1023));
   DecodeShared& sh = *reinterpret_cast<DecodeShared*>(tiles + kDecBufs * kDecTileBytes);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool consumer = warp < kDecWarps;
   const int T = a.T, H = a.H, F = a.F, E = a.E, k = a.k, Fs = a.Fs;
   const int Fm = max(F, Fs);
   const int G = gridDim.x;
   const int P = T * k;
 
   if (tid == 0) {
-    for (int b = 0; b < kDecBufs; ++b) mbar_init(&sh.bar[b], 1);
+    for (int b = 0; b < kDecBufs; ++b) {
+      mbar_init(&sh.full[b], 1);
+      mbar_init(&sh.empty[b], kDecWarps);
+    }
     sh.abort_flag = 0;
+    sh.h_ready = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
   // ---------------------------------------------------------------- R: router logits
-  // CTA b takes experts b, b + G, ...; thread i the rows 8i .. 8i+7 of each 2048-row
-  // stretch of H (one column element of W_router per row, a 16-byte load of x per token)
+  // CTA b takes experts b, b + G, ...; consumer thread i the rows 8i .. 8i+7 of each
+  // 2048-row stretch of H (one column element of W_router per row, a 16-byte load of x
+  // per token)
   for (int e = blockIdx.x; e < E; e += G) {
-    float acc[kDecMaxT];
+    if (consumer) {
+      float acc[kDecMaxT];
 #pragma unroll
-    for (int t = 0; t < kDecMaxT; ++t) acc[t] = 0.0f;
-    for (int r0 = tid * 8; r0 < H; r0 += kDecThreads * 8) {
-      float wv[8];
+      for (int t = 0; t < kDecMaxT; ++t) acc[t] = 0.0f;
+      for (int r0 = tid * 8; r0 < H; r0 += kDecThreads * 8) {
+        float wv[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) wv[q] = __bfloat162float(a.w_router[(int64_t)(r0 + q) * E + e]);
-      uint4 xr[kDecMaxT];  // every token's 16 bytes in flight before the sums
+        for (int q = 0; q < 8; ++q) wv[q] = __bfloat162float(a.w_router[(int64_t)(r0 + q) * E + e]);
+        uint4 xr[kDecMaxT];  // every token's 16 bytes in flight before the sums
 #pragma unroll
-      for (int t = 0; t < kDecMaxT; ++t)
-        xr[t] = t < T ? *reinterpret_cast<const uint4*>(a.x + (int64_t)t * H + r0) : make_uint4(0, 0, 0, 0);
+        for (int t = 0; t < kDecMaxT; ++t)
+          xr[t] = t < T ? *reinterpret_cast<const uint4*>(a.x + (int64_t)t * H + r0) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int t = 0; t < kDecMaxT; ++t) {
+          float xv[8];
+          bf16x8_to_f(xr[t], xv);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[t] = fmaf(xv[q], wv[q], acc[t]);
+        }
+      }
+      // a fixed butterfly inside each warp, then the eight warps in order, then the bias
 #pragma unroll
       for (int t = 0; t < kDecMaxT; ++t) {
-        float xv[8];
-        bf16x8_to_f(xr[t], xv);
+        float v = acc[t];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[t] = fmaf(xv[q], wv[q], acc[t]);
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0 && t < T) sh.red[warp][t] = v;
       }
-    }
-    // a fixed butterfly inside each warp, then the eight warps in order, then the bias
-#pragma unroll
-    for (int t = 0; t < kDecMaxT; ++t) {
-      float v = acc[t];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0 && t < T) sh.red[warp][t] = v;
     }
     __syncthreads();
     if (tid < T) {
       float l = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kDecThreads / 32; ++w) l += sh.red[w][tid];
+      for (int w = 0; w < kDecWarps; ++w) l += sh.red[w][tid];
       l += a.bias ? a.bias[e] : 0.0f;
       a.logits[tid * E + e] = l;
       if (a.user_logits) a.user_logits[tid * E + e] = l;
     }
     __syncthreads();
   }
-  if (!dec_grid_sync(a, sh, 1)) return;
+  dec_grid_arrive<true>(a, sh);
+  if (!dec_grid_wait<true>(a, sh, 1)) return;  // every thread, the producer warp too, leaves here
 
-  // ---------------------------------------------------------------- top-k and slots
+  // ---------------------------------------------------------------- K: top-k and slots
   {
     // warp w takes tokens w, w + 8, ...: lane l holds the logits of experts l, l + 32, ...
-    // as order-preserving keys (NaN reads as -inf, -0 as +0); each of k rounds takes the largest
-    // key still free, ties to the lower expert index, with two warp reductions
-    for (int t = warp; t < T; t += kDecThreads / 32) {
+    // as order-preserving keys (NaN reads as -inf, -0 as +0); each of k rounds takes the
+    // largest key still free, ties to the lower expert index, with two warp reductions
+    for (int t = warp; consumer && t < T; t += kDecWarps) {
       float v[kDecMaxE / 32];
       uint32_t key[kDecMaxE / 32];
 #pragma unroll
@@ -383,131 +431,43 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       sh.n_u = nu;
     }
     __syncthreads();
+    for (int u2 = tid; u2 < sh.n_u; u2 += kDecBlock)
+      for (int q = sh.ex_first[u2]; q < sh.ex_first[u2 + 1]; ++q) sh.slot_u[q] = u2;
+    __syncthreads();
   }
   const int n_routed = sh.n_routed, n_u = sh.n_u;
   auto slot_tok = [&](int s) { return s < P ? sh.slot_pair[s] / k : s - P; };
-  const int KC1 = (H + kDecStepRows - 1) / kDecStepRows;  // 256-row steps of H
 
-  Ring ring;
-  ring.next_issue = ring.next_use = ring.inflight = 0;
-#pragma unroll
-  for (int b = 0; b < kDecBufs; ++b) ring.phase[b] = 0;
-  auto slot_rows = [&](int u, int& s0, int& ns) {
-    s0 = sh.ex_first[u];
-    ns = sh.ex_first[u + 1] - s0;
-  };
-
-  // ---------------------------------------------------------------- G: x Wg, x Wu per 256-row chunk
-  // Steps (expert u, chunk kc of H, 64-column block fb of F_u, gate|up) in that order, an
-  // even share of them per CTA: at any moment the CTAs stream neighbouring column blocks
-  // of the same weight rows. Each step's 16 x 64 product (a 256-row partial sum) is
-  // stored in part_g; phase H adds the chunks.
-  {
-    const int nfb_r = F / 64, nfb_s = Fs / 64;
-    auto nfb = [&](int u) { return u < n_routed ? nfb_r : nfb_s; };
-    const int64_t per_r = (int64_t)KC1 * nfb_r * 2;
-    const int64_t total = (int64_t)n_routed * per_r + (Fs > 0 ? (int64_t)KC1 * nfb_s * 2 : 0);
-    const int64_t s0 = total * blockIdx.x / G, s1 = total * (blockIdx.x + 1) / G;
-    struct Cur {
-      int u, kc, fb, gu;
-    };
-    auto at = [&](int64_t g) {
-      Cur c;
-      int64_t rem;
-      if (g < (int64_t)n_routed * per_r) {
-        c.u = (int)(g / per_r);
-        rem = g - (int64_t)c.u * per_r;
-      } else {
-        c.u = n_routed;
-        rem = g - (int64_t)n_routed * per_r;
-      }
-      const int nf2 = nfb(c.u) * 2;
-      c.kc = (int)(rem / nf2);
-      const int r2 = (int)(rem - (int64_t)c.kc * nf2);
-      c.fb = r2 >> 1;
-      c.gu = r2 & 1;
-      return c;
-    };
-    auto advance = [&](Cur& c) {
-      if (++c.gu == 2) {
-        c.gu = 0;
-        if (++c.fb == nfb(c.u)) {
-          c.fb = 0;
-          if (++c.kc == KC1) {
-            c.kc = 0;
-            ++c.u;
-          }
-        }
-      }
-    };
-    auto issue = [&](const Cur& c) {
-      const int k0 = c.kc * kDecStepRows, nrows = min(kDecStepRows, H - k0);
-      if (c.u < n_routed)
-        ring_issue(sh, tiles, ring, c.gu ? &tm_up : &tm_gate, sh.ex_id[c.u] * H + k0, c.fb * 64, nrows);
-      else
-        ring_issue(sh, tiles, ring, c.gu ? &tm_sup : &tm_sgate, k0, c.fb * 64, nrows);
-    };
-    // x rows of expert u's tokens, the 256 columns of chunk kc
-    auto load_a = [&](int u, int kc, uint4 (&v)[2]) {
-      const int k0 = kc * kDecStepRows, nk = min(kDecStepRows, H - k0);
-      int sb, ns;
-      slot_rows(u, sb, ns);
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int idx = tid + q * kDecThreads, r = idx >> 5, c = idx & 31;
-        v[q] = make_uint4(0, 0, 0, 0);
-        if (r < ns && c * 8 < nk) v[q] = *reinterpret_cast<const uint4*>(a.x + (int64_t)slot_tok(sb + r) * H + k0 + c * 8);
-      }
-    };
-    if (s0 < s1) {
-      Cur ic = at(s0);
-      int64_t left = s1 - s0;
-      for (; ring.inflight < kDecBufs && left > 0; --left, advance(ic)) issue(ic);
-      Cur cc = at(s0);
-      // the A tile after the current one: (u, kc + 1), else (u + 1, 0), if this CTA reaches it
-      int nu = cc.u, nkc = cc.kc;
-      int64_t ng = s0 - (int64_t)((cc.fb * 2) + cc.gu);  // first step of the current A tile
-      uint4 av[2];
-      load_a(cc.u, cc.kc, av);
-      for (int64_t g = s0; g < s1; ++g, advance(cc)) {
-        if (g == s0 || (cc.fb == 0 && cc.gu == 0)) {
-          a_store(sh, av);  // the previous readers of the A tile passed the last barrier
-          ng += nfb(nu) * 2;
-          if (++nkc == KC1) {
-            nkc = 0;
-            ++nu;
-          }
-          if (ng < s1) load_a(nu, nkc, av);
-        }
-        uint32_t wt;
-        if (!ring_wait(sh, tiles, ring, a, wt)) return;
-        const int nrows = min(kDecStepRows, H - cc.kc * kDecStepRows);
-        float d0[4] = {0, 0, 0, 0}, d1[4] = {0, 0, 0, 0};
-        step_mma(sh, wt, nrows, d0, d1);
-        int sb, ns;
-        slot_rows(cc.u, sb, ns);
-        const int col = cc.fb * 64 + warp * 8 + (lane & 3) * 2, r0 = lane >> 2;
-        float* pg = a.part_g + ((int64_t)cc.kc * a.smax * 2 + cc.gu) * Fm + col;
-        if (r0 < ns)
-          *reinterpret_cast<float2*>(pg + (int64_t)(sb + r0) * 2 * Fm) = make_float2(d0[0] + d1[0], d0[1] + d1[1]);
-        if (r0 + 8 < ns)
-          *reinterpret_cast<float2*>(pg + (int64_t)(sb + r0 + 8) * 2 * Fm) =
-              make_float2(d0[2] + d1[2], d0[3] + d1[3]);
-        __syncthreads();  // this buffer (and, at an A step, the A tile) is free again
-        ring_release(ring);
-        if (left > 0) {
-          issue(ic);
-          advance(ic);
-          --left;
-        }
-      }
+  // ---------------------------------------------------------------- step lists of both roles
+  // G: units (expert u, column block cb of F_u); a unit's steps are its 32-row slices of
+  // H, gate then up, each step the whole width of the block. CTA c takes the steps
+  // [start(c), start(c + 1)) of all of them.
+  const int nbox_r = F / 64, nbox_s = Fs / 64;
+  const int ncb_r = (nbox_r + kDecGMaxBox - 1) / kDecGMaxBox, bpb_r = (nbox_r + ncb_r - 1) / ncb_r;
+  const int ncb_s = nbox_s > 0 ? (nbox_s + kDecGMaxBox - 1) / kDecGMaxBox : 0;
+  const int bpb_s = ncb_s > 0 ? (nbox_s + ncb_s - 1) / ncb_s : 1;
+  const int SG = 2 * (H / kDecGRows);  // steps per unit
+  const PhaseSteps phg{(int64_t)(n_routed * ncb_r + ncb_s) * SG, G};
+  const int64_t gs0 = phg.start(blockIdx.x), gs1 = phg.start(blockIdx.x + 1);
+  for (int c = tid; c <= G; c += kDecBlock) sh.cta_start[c] = (int)phg.start(c);
+  __syncthreads();  // every thread (the producer warp too) is still here
+  const PhaseTable pht{sh.cta_start, (uint32_t)phg.total, (uint32_t)G};
+  const int nG = (int)(gs1 - gs0);  // ring steps of this CTA's gate/up share
+  auto g_unit = [&](int i, int& u, int& cb, int& nbx, int& bpb) {
+    if (i < n_routed * ncb_r) {
+      u = i / ncb_r;
+      cb = i - u * ncb_r;
+      bpb = bpb_r;
+      nbx = min(bpb_r, nbox_r - cb * bpb_r);
+    } else {
+      u = n_routed;
+      cb = i - n_routed * ncb_r;
+      bpb = bpb_s;
+      nbx = min(bpb_s, nbox_s - cb * bpb_s);
     }
-  }
-
-  // ---------------------------------------------------------------- D: y = h Wd (its first copies)
-  // Units (expert u, 64 columns hb of H), CTA b taking units b, b + G, ...; each streams
-  // all F_u rows of W_down in 256-row steps. The first tiles are issued now, before the
-  // barriers, so they land while phase H runs.
+  };
+  // D: units (expert u, 64 columns hb of H), CTA b taking units b, b + G, ...; each
+  // streams all F_u rows of W_down in 256-row steps.
   const int nhb = H / 64;
   const int nunits_d = n_u * nhb;
   const int mine_d = nunits_d > (int)blockIdx.x ? (nunits_d - (int)blockIdx.x + G - 1) / G : 0;
@@ -523,93 +483,350 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       ++c.li;
     }
   };
-  auto d_issue = [&](const DCur& c) {
-    const int i = d_unit(c), u = i / nhb, hb = i % nhb, k0 = c.fk * kDecStepRows;
-    const int nrows = min(kDecStepRows, fu(u) - k0);
-    if (u < n_routed)
-      ring_issue(sh, tiles, ring, &tm_down, sh.ex_id[u] * F + k0, hb * 64, nrows);
-    else
-      ring_issue(sh, tiles, ring, &tm_sdown, k0, hb * 64, nrows);
-  };
-  DCur dic{0, 0};
-  dec_grid_arrive(a, sh);
-  for (; ring.inflight < kDecBufs && dic.li < mine_d; d_advance(dic)) d_issue(dic);
-  if (!dec_grid_wait(a, sh, 2)) {
-    if (tid == 0)  // let the copies already issued land before the shared memory is released
-      for (int q = 0; q < ring.inflight; ++q) {
-        const int bq = (ring.next_use + q) % kDecBufs;
-        mbar_wait_timed(&sh.bar[bq], ring.phase[bq], 200000000ull);
-      }
-    __syncthreads();
-    return;
-  }
 
-  // ---------------------------------------------------------------- H: h = silu(sum_kc g) * (sum_kc u)
-  {
-    const int S = n_routed > 0 ? sh.ex_first[n_u] : 0;
-    const int f8 = Fm / 8;
-    // item idx -> CTA idx % G, so that a few items still use many SMs
-    for (int idx = (int)blockIdx.x + G * tid; idx < S * f8; idx += G * kDecThreads) {
-      const int sl = idx / f8, f = (idx - sl * f8) * 8;
-      if (f >= (sl < P ? F : Fs)) continue;
-      float gs[8], us[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) gs[q] = us[q] = 0.0f;
-#pragma unroll 8
-      for (int kc = 0; kc < KC1; ++kc) {  // chunks in order
-        const float* pg = a.part_g + (((int64_t)kc * a.smax + sl) * 2) * Fm + f;
-        const float4 g0 = __ldcg(reinterpret_cast<const float4*>(pg));
-        const float4 g1 = __ldcg(reinterpret_cast<const float4*>(pg + 4));
-        const float4 u0 = __ldcg(reinterpret_cast<const float4*>(pg + Fm));
-        const float4 u1 = __ldcg(reinterpret_cast<const float4*>(pg + Fm + 4));
-        gs[0] += g0.x; gs[1] += g0.y; gs[2] += g0.z; gs[3] += g0.w;
-        gs[4] += g1.x; gs[5] += g1.y; gs[6] += g1.z; gs[7] += g1.w;
-        us[0] += u0.x; us[1] += u0.y; us[2] += u0.z; us[3] += u0.w;
-        us[4] += u1.x; us[5] += u1.y; us[6] += u1.z; us[7] += u1.w;
-      }
-      float h[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) h[q] = gs[q] * sigmoidf_(gs[q]) * us[q];
-      *reinterpret_cast<uint4*>(a.hbuf + (int64_t)sl * Fm + f) = f_to_bf16x8(h);
-    }
-  }
-  if (!dec_grid_sync(a, sh, 3)) {
-    if (tid == 0)
-      for (int q = 0; q < ring.inflight; ++q) {
-        const int bq = (ring.next_use + q) % kDecBufs;
-        mbar_wait_timed(&sh.bar[bq], ring.phase[bq], 200000000ull);
-      }
-    __syncthreads();
-    return;
-  }
-
-  // ---------------------------------------------------------------- D: y = h Wd
-  {
-    // h rows of unit i's slots, the 256 columns of step fk
-    auto load_a = [&](const DCur& c, uint4 (&v)[2]) {
-      const int u = d_unit(c) / nhb, k0 = c.fk * kDecStepRows, nk = min(kDecStepRows, fu(u) - k0);
-      int sb, ns;
-      slot_rows(u, sb, ns);
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int idx = tid + q * kDecThreads, r = idx >> 5, c8 = idx & 31;
-        v[q] = make_uint4(0, 0, 0, 0);
-        if (r < ns && c8 * 8 < nk)
-          v[q] = __ldcg(reinterpret_cast<const uint4*>(a.hbuf + (int64_t)(sb + r) * Fm + k0 + c8 * 8));
+  // ---------------------------------------------------------------- the producer warp
+  if (!consumer) {
+    if (lane != 0) return;
+    int j = 0;            // ring sequence number of the next copy
+    int ja = nG;          // sequence number of the next down step whose A tile is not issued
+    DCur ac{0, 0};        // its cursor
+    bool ok = true;
+    auto h_ready = [&]() {
+      int v;
+      asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(&sh.h_ready)) : "memory");
+      return v != 0;
+    };
+    // the A tile of down step ja: h rows of the unit's slots x the step's 256 columns;
+    // its arrival completes the step's barrier (the weights only announced their bytes)
+    auto issue_a = [&]() {
+      const int u = d_unit(ac) / nhb, k0 = ac.fk * kDecStepRows;
+      const int nbox = (min(kDecStepRows, fu(u) - k0) + 63) / 64;
+      const int b = ja % kDecBufs;
+      mbar_arrive_expect_tx(&sh.full[b], (uint32_t)(nbox * kDecDABoxRows * 128));
+      for (int x = 0; x < nbox; ++x)
+        tma_load_2d(smem_u32(tiles + b * kDecTileBytes + kDecDAOffset + x * kDecDABoxRows * 128), &tm_h,
+                    smem_u32(&sh.full[b]), k0 + x * 64, sh.ex_first[u]);
+      ++ja;
+      d_advance(ac);
+    };
+    // tile j's buffer free again (its previous use read by every consumer warp); A tiles
+    // of down steps already issued go out meanwhile, once h is ready
+    bool proxy_fenced = false;
+    auto pump_a = [&](int upto) {
+      if (ja < upto && h_ready()) {
+        if (!proxy_fenced) {  // h was written by generic stores in other CTAs
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          proxy_fenced = true;
+        }
+        while (ja < upto) issue_a();
       }
     };
+    auto acquire = [&](int jj) -> bool {
+      const uint32_t bar = smem_u32(&sh.empty[jj % kDecBufs]);
+      const uint32_t par = (uint32_t)(((jj / kDecBufs) & 1) ^ 1);
+      uint64_t t0 = 0;
+      uint32_t n = 0;
+      while (!mbar_try_wait(bar, par)) {
+        pump_a(jj);
+        if ((++n & 63u) == 0) {
+          if (*(volatile int*)&sh.abort_flag) return false;
+          const uint64_t now = globaltimer_ns();
+          if (t0 == 0)
+            t0 = now;
+          else if (now - t0 > kDecWaitNs) {
+            sh.abort_flag = 1;
+            set_status(a.status, MOE_ERR_TIMEOUT);
+            return false;
+          }
+        }
+      }
+      return true;
+    };
+    // gate/up steps
+    if (nG > 0) {
+      int ii = (int)(gs0 / SG), is = (int)(gs0 - (int64_t)ii * SG);
+      for (int q = 0; q < nG; ++q, ++j) {
+        if (!acquire(j)) {
+          ok = false;
+          break;
+        }
+        int u, cb, nbx, bpb;
+        g_unit(ii, u, cb, nbx, bpb);
+        const int r0 = (is >> 1) * kDecGRows, gu = is & 1;
+        const CUtensorMap* map = u < n_routed ? (gu ? &tm_up : &tm_gate) : (gu ? &tm_sup : &tm_sgate);
+        const int b = j % kDecBufs;
+        const int row0 = (u < n_routed ? sh.ex_id[u] * H : 0) + r0;
+        fence_async_smem();
+        mbar_arrive_expect_tx(&sh.full[b], (uint32_t)(nbx * kDecGBoxBytes));
+        for (int x = 0; x < nbx; ++x)
+          tma_load_2d(smem_u32(tiles + b * kDecTileBytes + x * kDecGBoxBytes), map, smem_u32(&sh.full[b]),
+                      (cb * bpb + x) * 64, row0);
+        if (++is == SG) {
+          is = 0;
+          ++ii;
+        }
+      }
+    }
+    // down steps: the weights as soon as a buffer is free, the A tiles once h is ready
+    for (DCur dc{0, 0}; ok && dc.li < mine_d; d_advance(dc), ++j) {
+      if (!acquire(j)) {
+        ok = false;
+        break;
+      }
+      const int i = d_unit(dc), u = i / nhb, hb = i % nhb, k0 = dc.fk * kDecStepRows;
+      const int nbox = (min(kDecStepRows, fu(u) - k0) + kDecBoxRows - 1) / kDecBoxRows;
+      const int b = j % kDecBufs;
+      const CUtensorMap* map = u < n_routed ? &tm_down : &tm_sdown;
+      const int row0 = (u < n_routed ? sh.ex_id[u] * F : 0) + k0;
+      fence_async_smem();
+      mbar_expect_tx(&sh.full[b], (uint32_t)(nbox * kDecBoxRows * 128));
+      for (int x = 0; x < nbox; ++x)
+        tma_load_2d(smem_u32(tiles + b * kDecTileBytes + x * kDecBoxRows * 128), map, smem_u32(&sh.full[b]), hb * 64,
+                    row0 + x * kDecBoxRows);
+      pump_a(j + 1);
+    }
+    // the A tiles still missing
+    if (ok) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ja < j) {
+        pump_a(j);
+        if (ja < j) {
+          if (*(volatile int*)&sh.abort_flag) {
+            ok = false;
+            break;
+          }
+          if (globaltimer_ns() - t0 > kDecWaitNs) {
+            sh.abort_flag = 1;
+            set_status(a.status, MOE_ERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+        }
+      }
+    }
+    if (!ok) {
+      // on the way out after a failed wait: every copy issued lands before the shared
+      // memory is released (a down step whose A tile never went out gets a plain arrival
+      // in its place, so that its barrier completes on the weights' bytes alone)
+      for (int q = j - kDecBufs < 0 ? 0 : j - kDecBufs; q < j; ++q) {
+        const int b = q % kDecBufs;
+        if (q >= ja) mbar_arrive(&sh.full[b]);
+        mbar_wait_timed(&sh.full[b], (uint32_t)((q / kDecBufs) & 1), 200000000ull);
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumers
+  auto slot_rows = [&](int u, int& s0, int& ns) {
+    s0 = sh.ex_first[u];
+    ns = sh.ex_first[u + 1] - s0;
+  };
+  int j = 0;  // ring sequence number of the next tile to read
+
+  // ---------------------------------------------------------------- G: x Wg, x Wu
+  // A unit's steps in this CTA are added in registers; at the end of the unit (or of the
+  // CTA's share) the sums go to part_g (a unit streamed whole) or to piece slot 2c (the
+  // CTA's first piece) or 2c + 1 (its last).
+  {
+    // A fragments of one 32-row slice of H (two k16 halves): rows = the unit's tokens
+    auto load_af = [&](int i, int st, uint32_t (&af)[2][4]) {
+      int u, cb, nbx, bpb;
+      g_unit(i, u, cb, nbx, bpb);
+      int sb, ns;
+      slot_rows(u, sb, ns);
+      const int g0 = lane >> 2, t4 = lane & 3, k0 = (st >> 1) * kDecGRows;
+      const __nv_bfloat16* x0 = a.x + (int64_t)slot_tok(sb + (g0 < ns ? g0 : 0)) * H;
+      const __nv_bfloat16* x1 = a.x + (int64_t)slot_tok(sb + (g0 + 8 < ns ? g0 + 8 : 0)) * H;
+#pragma unroll
+      for (int kq = 0; kq < 2; ++kq) {
+        const int kb = k0 + kq * 16 + 2 * t4;
+        af[kq][0] = g0 < ns ? *reinterpret_cast<const uint32_t*>(x0 + kb) : 0u;
+        af[kq][1] = g0 + 8 < ns ? *reinterpret_cast<const uint32_t*>(x1 + kb) : 0u;
+        af[kq][2] = g0 < ns ? *reinterpret_cast<const uint32_t*>(x0 + kb + 8) : 0u;
+        af[kq][3] = g0 + 8 < ns ? *reinterpret_cast<const uint32_t*>(x1 + kb + 8) : 0u;
+      }
+    };
+    float ag[kDecGMaxBox][4], au[kDecGMaxBox][4];
+#pragma unroll
+    for (int x = 0; x < kDecGMaxBox; ++x)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) ag[x][q] = au[x][q] = 0.0f;
+    auto flush = [&](int i) {
+      int u, cb, nbx, bpb;
+      g_unit(i, u, cb, nbx, bpb);
+      int sb, ns;
+      slot_rows(u, sb, ns);
+      const int64_t ub = (int64_t)i * SG, ue = ub + SG;
+      const bool whole = ub >= gs0 && ue <= gs1;
+      const int ps = ub <= gs0 ? 2 * (int)blockIdx.x : 2 * (int)blockIdx.x + 1;
+      const int r0 = lane >> 2, cq = warp * 8 + (lane & 3) * 2;
+#pragma unroll
+      for (int x = 0; x < kDecGMaxBox; ++x) {
+        if (x < nbx) {
+#pragma unroll
+          for (int gu = 0; gu < 2; ++gu) {
+#pragma unroll
+            for (int h8 = 0; h8 < 2; ++h8) {
+              const int r = r0 + 8 * h8;
+              if (r < ns) {
+                const float v0 = gu ? au[x][2 * h8] : ag[x][2 * h8];
+                const float v1 = gu ? au[x][2 * h8 + 1] : ag[x][2 * h8 + 1];
+                float* dst = whole ? a.part_g + ((int64_t)(sb + r) * 2 + gu) * Fm + (cb * bpb + x) * 64 + cq
+                                   : a.piece_g + (((int64_t)ps * 2 + gu) * T + r) * kDecGMaxCols + x * 64 + cq;
+                *reinterpret_cast<float2*>(dst) = make_float2(v0, v1);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ag[x][q] = au[x][q] = 0.0f;
+      }
+    };
+    if (nG > 0) {
+      int ci = (int)(gs0 / SG), cs = (int)(gs0 - (int64_t)ci * SG);  // unit and step of the tile
+      int ai = ci, as = cs & ~1;  // the slice whose A fragments are in an
+      uint32_t af[2][4], an[2][4];
+      load_af(ai, as, an);
+      for (int64_t g = gs0; g < gs1; ++g, ++j) {
+        if (g == gs0 || (cs & 1) == 0) {  // a new 32-row slice: its A fragments, and the next slice's in flight
+#pragma unroll
+          for (int kq = 0; kq < 2; ++kq)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) af[kq][q] = an[kq][q];
+          as += 2;
+          if (as == SG) {
+            as = 0;
+            ++ai;
+          }
+          if ((int64_t)ai * SG + as < gs1) load_af(ai, as, an);
+        }
+        if (!wait_full(sh, a, j)) break;  // the barrier below makes every warp leave
+        int u, cb, nbx, bpb;
+        g_unit(ci, u, cb, nbx, bpb);
+        const uint32_t wt = smem_u32(tiles + (j % kDecBufs) * kDecTileBytes);
+        if (cs & 1)
+          step_mma_rows(wt, nbx, af, au);
+        else
+          step_mma_rows(wt, nbx, af, ag);
+        release(sh, j);
+        if (g + 1 == gs1 || cs + 1 == SG) flush(ci);
+        if (++cs == SG) {
+          cs = 0;
+          ++ci;
+        }
+      }
+    }
+  }
+  dec_grid_arrive<false>(a, sh);
+  if (!dec_grid_wait<false>(a, sh, 2)) return;
+
+  // ---------------------------------------------------------------- H: h = silu(g) * u
+  // Item (slot sl, 4 columns f) with 8 lanes: for a unit one CTA streamed whole lane 0
+  // reads part_g; for a split unit lane l adds the pieces of CTAs clo + l, clo + l + 8,
+  // ... and a fixed butterfly adds the eight lanes.
+  {
+    const int S = sh.ex_first[n_u];
+    const int f4 = Fm / 4, nitems = S * f4;
+    const int grp = tid >> 3, sub = tid & 7;  // 32 groups per CTA
+    const int passes = (nitems + 32 * G - 1) / (32 * G);
+    for (int p = 0; p < passes; p += 2) {  // two items per group in flight
+      int sl[2], fc[2];
+      bool valid[2];
+      float4 pgv[2][4], puv[2][4];
+#pragma unroll
+      for (int b2 = 0; b2 < 2; ++b2) {
+        const int item = (int)blockIdx.x + G * (32 * (p + b2) + grp);
+        sl[b2] = item / f4;
+        fc[b2] = (item - sl[b2] * f4) * 4;
+        valid[b2] = p + b2 < passes && item < nitems;
+        int u = 0;
+        if (valid[b2]) {
+          u = sh.slot_u[sl[b2]];
+          valid[b2] = fc[b2] < (u < n_routed ? F : Fs);
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) pgv[b2][m] = puv[b2][m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!valid[b2]) continue;
+        const int f = fc[b2];
+        const int bpb = u < n_routed ? bpb_r : bpb_s;
+        const int cb = (f >> 6) / bpb;
+        const int i = (u < n_routed ? u * ncb_r : n_routed * ncb_r) + cb;
+        const int ub = i * SG;
+        const int clo = pht.cta_of((uint32_t)ub), chi = pht.cta_of((uint32_t)(ub + SG - 1));
+        if (clo == chi) {
+          if (sub == 0) {
+            const float* pg = a.part_g + (int64_t)sl[b2] * 2 * Fm + f;
+            pgv[b2][0] = __ldcg(reinterpret_cast<const float4*>(pg));
+            puv[b2][0] = __ldcg(reinterpret_cast<const float4*>(pg + Fm));
+          }
+        } else {
+          const int row = sl[b2] - sh.ex_first[u], colp = f - cb * bpb * 64;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {  // up to 32 pieces in one round of loads
+            const int q = clo + sub + 8 * m;
+            if (q <= chi && pht.start[q] < pht.start[q + 1]) {
+              const int ps = (q > clo || pht.start[clo] == ub) ? 2 * q : 2 * q + 1;
+              const float* pp = a.piece_g + ((int64_t)ps * 2 * T + row) * kDecGMaxCols + colp;
+              pgv[b2][m] = __ldcg(reinterpret_cast<const float4*>(pp));
+              puv[b2][m] = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)T * kDecGMaxCols));
+            }
+          }
+          for (int q0 = clo + sub + 32; q0 <= chi; q0 += 8) {  // more than 32 pieces
+            if (pht.start[q0] < pht.start[q0 + 1]) {
+              const float* pp = a.piece_g + ((int64_t)2 * q0 * 2 * T + row) * kDecGMaxCols + colp;
+              const float4 g4 = __ldcg(reinterpret_cast<const float4*>(pp));
+              const float4 u4 = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)T * kDecGMaxCols));
+              pgv[b2][3].x += g4.x; pgv[b2][3].y += g4.y; pgv[b2][3].z += g4.z; pgv[b2][3].w += g4.w;
+              puv[b2][3].x += u4.x; puv[b2][3].y += u4.y; puv[b2][3].z += u4.z; puv[b2][3].w += u4.w;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int b2 = 0; b2 < 2; ++b2) {
+        float4 gs = pgv[b2][0], us = puv[b2][0];
+#pragma unroll
+        for (int m = 1; m < 4; ++m) {
+          gs.x += pgv[b2][m].x; gs.y += pgv[b2][m].y; gs.z += pgv[b2][m].z; gs.w += pgv[b2][m].w;
+          us.x += puv[b2][m].x; us.y += puv[b2][m].y; us.z += puv[b2][m].z; us.w += puv[b2][m].w;
+        }
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) {  // the eight lanes of the group, a fixed tree
+          gs.x += __shfl_xor_sync(0xffffffffu, gs.x, o);
+          gs.y += __shfl_xor_sync(0xffffffffu, gs.y, o);
+          gs.z += __shfl_xor_sync(0xffffffffu, gs.z, o);
+          gs.w += __shfl_xor_sync(0xffffffffu, gs.w, o);
+          us.x += __shfl_xor_sync(0xffffffffu, us.x, o);
+          us.y += __shfl_xor_sync(0xffffffffu, us.y, o);
+          us.z += __shfl_xor_sync(0xffffffffu, us.z, o);
+          us.w += __shfl_xor_sync(0xffffffffu, us.w, o);
+        }
+        if (valid[b2] && sub == 0) {
+          const float h0 = gs.x * sigmoidf_(gs.x) * us.x, h1 = gs.y * sigmoidf_(gs.y) * us.y;
+          const float h2 = gs.z * sigmoidf_(gs.z) * us.z, h3 = gs.w * sigmoidf_(gs.w) * us.w;
+          __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(a.hbuf + (int64_t)sl[b2] * Fm + fc[b2]);
+          dst[0] = __floats2bfloat162_rn(h0, h1);
+          dst[1] = __floats2bfloat162_rn(h2, h3);
+        }
+      }
+    }
+    // h is read next by the tensor-memory-access copies of other CTAs
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+  }
+  dec_grid_arrive<false>(a, sh);
+  if (!dec_grid_wait<false>(a, sh, 3)) return;
+  if (tid == 0) asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(&sh.h_ready)), "r"(1) : "memory");
+
+  // ---------------------------------------------------------------- D: y = h W_down
+  {
     float d0[4] = {0, 0, 0, 0}, d1[4] = {0, 0, 0, 0};
-    uint4 av[2];
-    DCur cc{0, 0}, ac{0, 0};
-    if (mine_d > 0) load_a(ac, av);
-    for (; cc.li < mine_d; d_advance(cc)) {
-      a_store(sh, av);  // every step starts an A tile; its previous readers passed the last barrier
-      d_advance(ac);
-      if (ac.li < mine_d) load_a(ac, av);
-      uint32_t wt;
-      if (!ring_wait(sh, tiles, ring, a, wt)) return;
+    for (DCur cc{0, 0}; cc.li < mine_d; d_advance(cc), ++j) {
+      if (!wait_full(sh, a, j)) break;  // the barrier below makes every warp leave
       const int i = d_unit(cc), u = i / nhb;
-      step_mma(sh, wt, min(kDecStepRows, fu(u) - cc.fk * kDecStepRows), d0, d1);
+      const uint32_t wt = smem_u32(tiles + (j % kDecBufs) * kDecTileBytes);
+      step_mma_down(wt, min(kDecStepRows, fu(u) - cc.fk * kDecStepRows), d0, d1);
+      release(sh, j);
       if (cc.fk + 1 == kc2(u)) {  // the unit's last step: its y rows
         const int hb = i % nhb;
         int sb, ns;
@@ -623,15 +840,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) d0[q] = d1[q] = 0.0f;
       }
-      __syncthreads();  // this buffer and the A tile are free again
-      ring_release(ring);
-      if (dic.li < mine_d) {
-        d_issue(dic);
-        d_advance(dic);
-      }
     }
   }
-  if (!dec_grid_sync(a, sh, 4)) return;
+  dec_grid_arrive<false>(a, sh);
+  if (!dec_grid_wait<false>(a, sh, 4)) return;
 
   // ---------------------------------------------------------------- C: combine
   for (int idx = blockIdx.x * kDecThreads + tid; idx < T * (H / 4); idx += G * kDecThreads) {
@@ -678,13 +890,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 dec_encode_fn() {
   return fn;
 }
 
-// [rows, cols] bf16, boxes of 64 rows x 64 columns, 128-byte swizzle
-static bool dec_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
+// [rows, cols] bf16, boxes of box_rows rows x 64 columns, 128-byte swizzle
+static bool dec_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
   auto fn = dec_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kDecBoxRows};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -695,9 +907,10 @@ static bool dec_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols)
 static int64_t dec_slots(int64_t T, int64_t k) { return T * k + T; }
 
 size_t decode_scratch_bytes(int64_t T, int64_t H, int64_t F, int64_t E, int64_t k, int64_t Fs) {
-  const int64_t Fm = F > Fs ? F : Fs, S = dec_slots(T, k), KC1 = (H + kDecStepRows - 1) / kDecStepRows;
+  const int64_t Fm = F > Fs ? F : Fs, S = dec_slots(T, k);
   auto up = [](int64_t n) { return (size_t)((n + 255) / 256 * 256); };
-  return up(T * E * 4) + up(S * Fm * 2) + up(S * H * 4) + up(KC1 * S * 2 * Fm * 4) + 256;
+  return up(T * E * 4) + up(S * Fm * 2) + up(S * H * 4) + up(S * 2 * Fm * 4) +
+         up((int64_t)2 * kDecMaxGrid * 2 * T * kDecGMaxCols * 4) + 256;
 }
 
 bool decode_supported(int64_t T, int64_t H, int64_t F, int64_t E, int64_t k, int64_t Fs) {
@@ -710,7 +923,7 @@ cudaError_t launch_decode_fwd(int T, int H, int F, int E, int k, int Fs, const v
                               const void* ws_gate, const void* ws_up, const void* ws_down, void* y, int* topk_idx,
                               float* topk_w, int* user_idx, float* user_w, float* user_logits, void* scratch,
                               int* status, int num_sms, cudaStream_t st) {
-  const int64_t Fm = F > Fs ? F : Fs, S = dec_slots(T, k), KC1 = (H + kDecStepRows - 1) / kDecStepRows;
+  const int64_t Fm = F > Fs ? F : Fs, S = dec_slots(T, k);
   auto up = [](int64_t n) { return (int64_t)((n + 255) / 256 * 256); };
   char* b = static_cast<char*>(scratch);
   DecodeArgs a;
@@ -731,19 +944,22 @@ cudaError_t launch_decode_fwd(int T, int H, int F, int E, int k, int Fs, const v
   a.ypair = reinterpret_cast<float*>(b);
   b += up(S * H * 4);
   a.part_g = reinterpret_cast<float*>(b);
-  a.smax = (int)S;
-  b += up(KC1 * S * 2 * Fm * 4);
+  b += up(S * 2 * Fm * 4);
+  a.piece_g = reinterpret_cast<float*>(b);
+  b += up((int64_t)2 * kDecMaxGrid * 2 * T * kDecGMaxCols * 4);
   a.sync = reinterpret_cast<unsigned*>(b);
   a.status = status;
   cudaError_t e = cudaMemsetAsync(a.sync, 0, sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
-  CUtensorMap mg, mu, md, msg, msu, msd;
-  bool ok = dec_map(&mg, w_gate, (int64_t)E * H, F) && dec_map(&mu, w_up, (int64_t)E * H, F) &&
-            dec_map(&md, w_down, (int64_t)E * F, H);
+  CUtensorMap mg, mu, md, msg, msu, msd, mh;
+  bool ok = dec_map(&mg, w_gate, (int64_t)E * H, F, kDecGRows) && dec_map(&mu, w_up, (int64_t)E * H, F, kDecGRows) &&
+            dec_map(&md, w_down, (int64_t)E * F, H, kDecBoxRows);
   if (Fs > 0)
-    ok = ok && dec_map(&msg, ws_gate, H, Fs) && dec_map(&msu, ws_up, H, Fs) && dec_map(&msd, ws_down, Fs, H);
+    ok = ok && dec_map(&msg, ws_gate, H, Fs, kDecGRows) && dec_map(&msu, ws_up, H, Fs, kDecGRows) &&
+         dec_map(&msd, ws_down, Fs, H, kDecBoxRows);
   else
     msg = msu = msd = mg;  // unused without a shared expert
+  ok = ok && dec_map(&mh, a.hbuf, S, Fm, kDecDABoxRows);  // the A tiles of the down steps
   if (!ok) return cudaErrorInvalidValue;
   const int smem = kDecBufs * kDecTileBytes + (int)sizeof(DecodeShared) + 1024;
   // once per device: the shared-memory attribute, and that one CTA per SM fits (all CTAs
@@ -759,14 +975,15 @@ cudaError_t launch_decode_fwd(int T, int H, int F, int E, int k, int Fs, const v
       e = cudaFuncSetAttribute(k_decode_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       int per_sm = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode_fwd, kDecThreads, smem);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode_fwd, kDecBlock, smem);
       if (e != cudaSuccess) return e;
       if (per_sm < 1) return cudaErrorInvalidConfiguration;
       if (dev >= 0 && dev < 64) ready[dev] = true;
     }
   }
-  void* args[] = {&mg, &mu, &md, &msg, &msu, &msd, &a};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_decode_fwd), dim3(num_sms), dim3(kDecThreads),
+  void* args[] = {&mg, &mu, &md, &msg, &msu, &msd, &mh, &a};
+  const int grid = num_sms < kDecMaxGrid ? num_sms : kDecMaxGrid;  // piece slots exist for kDecMaxGrid CTAs
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_decode_fwd), dim3(grid), dim3(kDecBlock),
                                      args, (size_t)smem, st);
 }
 
