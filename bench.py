@@ -41,6 +41,7 @@ def parse(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-decode-leg", action="store_true", help="skip the decode-sized forward leg")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="oracle time budget for cpu_baseline")
     return ap.parse_args(argv)
 
@@ -488,7 +489,7 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "copies": "pinned host buffers; on a second stream, overlapped with the neighbouring steps"},
             "roofline": roof}
-    if world == 1:
+    if world == 1 and not args.no_decode_leg:
         line["decode"] = decode_leg(w, inp, dev, peaks)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, args.seed, args.cpu_budget_s)
