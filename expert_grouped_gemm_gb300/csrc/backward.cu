@@ -537,9 +537,9 @@ __global__ void __launch_bounds__(256) k_dx_reduce_k8(const __nv_bfloat16* __res
                                                       const __nv_bfloat16* __restrict__ wrT,
                                                       const __nv_bfloat16* __restrict__ sh_dx, int T, int H, int k,
                                                       __nv_bfloat16* __restrict__ dx) {
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
   const int nv = H / 8;
-  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
+  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
     int c = -1, ex = 0;
     float d = 0.0f;
     if (lane < k) {
@@ -594,11 +594,18 @@ cudaError_t launch_dx_reduce(const void* dx_pair, const int* crow_of_pair, const
                              const void* wrT, const void* sh_dx, int T, int H, int k, void* dx, int num_sms,
                              cudaStream_t st) {
   if (sizeof(TIO) == 2 && k <= 8) {
-    int per_sm = 0;  // grid-stride over tokens with as many blocks as fit at once
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_dx_reduce_k8, 256, 0) != cudaSuccess || per_sm < 1)
+    // a warp per token in blocks of two warps, grid-stride with as many blocks as fit at
+    // once: tokens spread over the SMs a warp at a time (blocks of eight warps left a
+    // quarter of the SMs one block behind)
+    constexpr int kThreads = 64;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_dx_reduce_k8, kThreads, 0) != cudaSuccess ||
+        per_sm < 1)
       per_sm = 1;
-    const int g = (int)std::max<int64_t>(1, std::min<int64_t>(((int64_t)T + 7) / 8, (int64_t)num_sms * per_sm));
-    k_dx_reduce_k8<<<g, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(dx_pair), crow_of_pair, topk_idx, dl_sel,
+    const int wpb = kThreads / 32;
+    const int g =
+        (int)std::max<int64_t>(1, std::min<int64_t>(((int64_t)T + wpb - 1) / wpb, (int64_t)num_sms * per_sm));
+    k_dx_reduce_k8<<<g, kThreads, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(dx_pair), crow_of_pair, topk_idx, dl_sel,
                                       reinterpret_cast<const __nv_bfloat16*>(wrT),
                                       reinterpret_cast<const __nv_bfloat16*>(sh_dx), T, H, k,
                                       reinterpret_cast<__nv_bfloat16*>(dx));
