@@ -6,8 +6,8 @@
 // short kernels whose launch, prologue and pipeline fill cost more than the stream.
 // Here one cooperative launch (one CTA per SM, every CTA resident) runs these phases,
 // separated by grid-wide barriers:
-//   R  router logits: CTA b computes logits[t, b], logits[t, b + G], ... over all of H
-//      (CUDA cores), with the bias added;
+//   R  router logits: CTA (16-expert group, quarter of H) computes its block of
+//      W_r^T x^T with mma.sync, a partial sum the top-k warps add in a fixed order;
 //   K  every CTA takes the top-k and the renormalised softmax weights of every token
 //      and builds the same slot table (the routed (token, expert) pairs sorted by
 //      expert then token, then one slot per token for the shared expert);
@@ -57,6 +57,7 @@ constexpr int kDecBoxRows = 64;
 constexpr int kDecDABoxRows = 16;
 constexpr int kDecDAOffset = 32768;
 constexpr int kDecMaxE = 256;
+constexpr int kDecRSlices = 4;  // router: row slices of H, each summed by its own CTAs
 constexpr int kDecMaxK = 16;  // T * k <= 256: one thread per routed pair when ranking them
 constexpr int kDecMaxH = 4096;
 constexpr int kDecMaxGrid = 256;  // CTAs of one launch at most (one per SM)
@@ -73,7 +74,7 @@ struct DecodeArgs {
   int* user_idx;      // nullable
   float* user_w;      // nullable
   float* user_logits; // nullable [T,E]
-  float* logits;      // [T][E] biased fp32 logits
+  float* logits;      // [kDecRSlices][T][E]: router partial sums over the row slices of H
   __nv_bfloat16* hbuf;  // [slots][Fm]
   float* ypair;       // [slots][H]
   float* part_g;      // [slots][gate, up][Fm]: x Wg and x Wu of a unit streamed by one CTA
@@ -83,7 +84,6 @@ struct DecodeArgs {
 };
 
 struct DecodeShared {
-  float red[kDecWarps][kDecMaxT];            // router: one partial sum per warp and token
   int s_idx[kDecMaxT * kDecMaxK];
   float s_w[kDecMaxT * kDecMaxK];
   int slot_pair[kDecMaxT * kDecMaxK];        // routed slot -> pair t*k + j
@@ -215,48 +215,61 @@ __device__ __forceinline__ void release(DecodeShared& sh, int j) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.empty[j % kDecBufs]);
 }
 
-// acc[x] += A (16 rows x 32 columns, fragments in registers) x (box x of the tile at wt:
-// 32 rows x 64 columns) for the nbx boxes of a gate/up step: warp w takes columns
-// 8w .. 8w+7 of every box, so its nbx accumulators are independent chains.
-__device__ __forceinline__ void step_mma_rows(uint32_t wt, int nbx, const uint32_t (&af)[2][4],
-                                              float (&acc)[kDecGMaxBox][4]) {
+// A gate/up step is read out of its tile into registers first (bf: box x, k16 half kq),
+// so that the tile can be freed before the multiplications: warp w takes columns
+// 8w .. 8w+7 of every box.
+__device__ __forceinline__ void step_load_rows(uint32_t wt, int nbx, uint32_t (&bf)[2][kDecGMaxBox][2]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int kq = 0; kq < 2; ++kq) {
     const int br = kq * 16 + (lane & 15);
     const uint32_t boff = (uint32_t)(br * 128 + ((warp ^ (br & 7)) << 4));
 #pragma unroll
-    for (int x = 0; x < kDecGMaxBox; ++x) {
-      if (x < nbx) {
-        uint32_t b0, b1;
-        ldsm_x2_trans(wt + (uint32_t)(x * kDecGBoxBytes) + boff, b0, b1);
-        mma_16816(acc[x], af[kq][0], af[kq][1], af[kq][2], af[kq][3], b0, b1);
-      }
-    }
+    for (int x = 0; x < kDecGMaxBox; ++x)
+      if (x < nbx) ldsm_x2_trans(wt + (uint32_t)(x * kDecGBoxBytes) + boff, bf[kq][x][0], bf[kq][x][1]);
   }
 }
+// acc[x] += A (16 rows x 32 columns, fragments in registers) x (box x: 32 rows x 64 columns)
+// for the nbx boxes of the step; the nbx accumulators are independent chains.
+__device__ __forceinline__ void step_mma_rows(int nbx, const uint32_t (&af)[2][4], const uint32_t (&bf)[2][kDecGMaxBox][2],
+                                              float (&acc)[kDecGMaxBox][4]) {
+#pragma unroll
+  for (int kq = 0; kq < 2; ++kq)
+#pragma unroll
+    for (int x = 0; x < kDecGMaxBox; ++x)
+      if (x < nbx) mma_16816(acc[x], af[kq][0], af[kq][1], af[kq][2], af[kq][3], bf[kq][x][0], bf[kq][x][1]);
+}
 
-// d0 + d1 += (the step's A tile at wt + kDecDAOffset: 16 rows x nrows columns, four
-// swizzled 16-row boxes) x (the weight tile at wt: nrows rows x 64 columns): warp w
-// takes columns 8w .. 8w+7; even 16-row slices go to d0, odd ones to d1.
-__device__ __forceinline__ void step_mma_down(uint32_t wt, int nrows, float (&d0)[4], float (&d1)[4]) {
+// A down step read out of its tile into registers (16-row slice h of the nrows rows: A
+// fragments fa[h] from the step's A tile at wt + kDecDAOffset, four swizzled 16-row
+// boxes; B fragments fb[h] of the weight tile at wt), so that the tile can be freed
+// before the multiplications. nrows is a multiple of 64.
+__device__ __forceinline__ void step_load_down(uint32_t wt, int nrows, uint32_t (&fa)[16][4], uint32_t (&fb)[16][2]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t at = wt + kDecDAOffset;
   const int ar = lane & 15;
-#pragma unroll 2
-  for (int kk = 0; kk < nrows; kk += 32) {
-    uint32_t a[2][4], b[2][2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int k0 = kk + 16 * h;
+  for (int h = 0; h < 16; ++h) {
+    const int k0 = 16 * h;
+    if (k0 < nrows) {
       const int chunk = ((k0 & 63) >> 3) + (lane >> 4);  // 16-byte chunk of the A box row
-      ldsm_x4(at + (uint32_t)((k0 >> 6) * (kDecDABoxRows * 128) + ar * 128 + ((chunk ^ (ar & 7)) << 4)), a[h][0],
-              a[h][1], a[h][2], a[h][3]);
+      ldsm_x4(at + (uint32_t)((k0 >> 6) * (kDecDABoxRows * 128) + ar * 128 + ((chunk ^ (ar & 7)) << 4)), fa[h][0],
+              fa[h][1], fa[h][2], fa[h][3]);
       const int br = k0 + (lane & 15);
-      ldsm_x2_trans(wt + (uint32_t)(br * 128 + ((warp ^ (br & 7)) << 4)), b[h][0], b[h][1]);
+      ldsm_x2_trans(wt + (uint32_t)(br * 128 + ((warp ^ (br & 7)) << 4)), fb[h][0], fb[h][1]);
     }
-    mma_16816(d0, a[0][0], a[0][1], a[0][2], a[0][3], b[0][0], b[0][1]);
-    mma_16816(d1, a[1][0], a[1][1], a[1][2], a[1][3], b[1][0], b[1][1]);
+  }
+}
+// d0 + d1 += A x B over the step's 16-row slices: warp w takes columns 8w .. 8w+7; even
+// slices go to d0, odd ones to d1.
+__device__ __forceinline__ void step_mma_down(int nrows, const uint32_t (&fa)[16][4], const uint32_t (&fb)[16][2],
+                                              float (&d0)[4], float (&d1)[4]) {
+#pragma unroll
+  for (int h = 0; h < 16; h += 2) {
+    if (16 * h < nrows) {
+      mma_16816(d0, fa[h][0], fa[h][1], fa[h][2], fa[h][3], fb[h][0], fb[h][1]);
+      mma_16816(d1, fa[h + 1][0], fa[h + 1][1], fa[h + 1][2], fa[h + 1][3], fb[h + 1][0], fb[h + 1][1]);
+    }
   }
 }
 
@@ -288,49 +301,62 @@ __global__ void __launch_bounds__(kDecBlock, 1)
   __syncthreads();
 
   // ---------------------------------------------------------------- R: router logits
-  // CTA b takes experts b, b + G, ...; consumer thread i the rows 8i .. 8i+7 of each
-  // 2048-row stretch of H (one column element of W_router per row, a 16-byte load of x
-  // per token)
-  for (int e = blockIdx.x; e < E; e += G) {
-    if (consumer) {
-      float acc[kDecMaxT];
+  // CTA (expert group eg of 16 experts, row slice sl of H) computes the 16 x T block of
+  // logits^T = W_r^T x^T over its rows with mma.sync (experts as M, tokens as N), warp w
+  // taking the 16-row blocks w, w + 8, ...; the eight warps are added in order and the
+  // partial goes to a.logits[sl]. A slice's rows are read by the CTAs of all expert
+  // groups at once, 32 bytes of each W_r row per CTA, so DRAM sees whole rows.
+  {
+    const int EG = (E + 15) / 16;
+    const int nkb = H / 16, kbs = (nkb + kDecRSlices - 1) / kDecRSlices;  // 16-row blocks per slice
+    for (int rb = blockIdx.x; rb < EG * kDecRSlices; rb += G) {
+      const int eg = rb % EG, sl = rb / EG;
+      const int kb0 = sl * kbs, kb1 = min(nkb, kb0 + kbs);
+      const int g0 = lane >> 2, t4 = lane & 3;
+      const int ea = eg * 16 + g0, eb = ea + 8;  // the two experts (M rows) of this lane
+      float c[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+      if (consumer) {
+        auto wpair = [&](int e, int k) -> uint32_t {  // W_r[k][e], W_r[k + 1][e] packed
+          if (e >= E) return 0u;
+          const uint16_t lo = reinterpret_cast<const uint16_t*>(a.w_router)[(int64_t)k * E + e];
+          const uint16_t hi = reinterpret_cast<const uint16_t*>(a.w_router)[(int64_t)(k + 1) * E + e];
+          return (uint32_t)lo | ((uint32_t)hi << 16);
+        };
+#pragma unroll 4
+        for (int kb = kb0 + warp; kb < kb1; kb += kDecWarps) {
+          const int k0 = kb * 16 + 2 * t4;
+          const uint32_t a0 = wpair(ea, k0), a1 = wpair(eb, k0), a2 = wpair(ea, k0 + 8), a3 = wpair(eb, k0 + 8);
 #pragma unroll
-      for (int t = 0; t < kDecMaxT; ++t) acc[t] = 0.0f;
-      for (int r0 = tid * 8; r0 < H; r0 += kDecThreads * 8) {
-        float wv[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) wv[q] = __bfloat162float(a.w_router[(int64_t)(r0 + q) * E + e]);
-        uint4 xr[kDecMaxT];  // every token's 16 bytes in flight before the sums
-#pragma unroll
-        for (int t = 0; t < kDecMaxT; ++t)
-          xr[t] = t < T ? *reinterpret_cast<const uint4*>(a.x + (int64_t)t * H + r0) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int t = 0; t < kDecMaxT; ++t) {
-          float xv[8];
-          bf16x8_to_f(xr[t], xv);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc[t] = fmaf(xv[q], wv[q], acc[t]);
+          for (int nt = 0; nt < 2; ++nt) {
+            const int t = nt * 8 + g0;
+            if (nt * 8 < T) {
+              uint32_t b0 = 0u, b1 = 0u;
+              if (t < T) {
+                b0 = *reinterpret_cast<const uint32_t*>(a.x + (int64_t)t * H + k0);
+                b1 = *reinterpret_cast<const uint32_t*>(a.x + (int64_t)t * H + k0 + 8);
+              }
+              mma_16816(c[nt], a0, a1, a2, a3, b0, b1);
+            }
+          }
         }
       }
-      // a fixed butterfly inside each warp, then the eight warps in order, then the bias
+      // the warps' fragments, added in warp order (the idle ring holds them)
+      float* red = reinterpret_cast<float*>(tiles);
+      if (consumer)
 #pragma unroll
-      for (int t = 0; t < kDecMaxT; ++t) {
-        float v = acc[t];
+        for (int q = 0; q < 8; ++q) red[(warp * 32 + lane) * 8 + q] = c[q >> 2][q & 3];
+      __syncthreads();
+      if (consumer) {
+        const int ln = tid >> 3, q = tid & 7, nt = q >> 2, ci = q & 3;
+        float v = 0.0f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0 && t < T) sh.red[warp][t] = v;
+        for (int w = 0; w < kDecWarps; ++w) v += red[(w * 32 + ln) * 8 + q];
+        // fragment element ci of lane ln: expert row (ln >> 2) + 8 (ci >> 1), token 2 (ln & 3) + (ci & 1)
+        const int e = eg * 16 + (ln >> 2) + 8 * (ci >> 1), t = nt * 8 + 2 * (ln & 3) + (ci & 1);
+        if (e < E && t < T) a.logits[((int64_t)sl * T + t) * E + e] = v;
       }
+      __syncthreads();  // the ring is idle until the first copies; its readers are done here
     }
-    __syncthreads();
-    if (tid < T) {
-      float l = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) l += sh.red[w][tid];
-      l += a.bias ? a.bias[e] : 0.0f;
-      a.logits[tid * E + e] = l;
-      if (a.user_logits) a.user_logits[tid * E + e] = l;
-    }
-    __syncthreads();
   }
   dec_grid_arrive<true>(a, sh);
   if (!dec_grid_wait<true>(a, sh, 1)) return;  // every thread, the producer warp too, leaves here
@@ -343,10 +369,24 @@ __global__ void __launch_bounds__(kDecBlock, 1)
     for (int t = warp; consumer && t < T; t += kDecWarps) {
       float v[kDecMaxE / 32];
       uint32_t key[kDecMaxE / 32];
+      float ps[kDecRSlices][kDecMaxE / 32];  // every slice's partial in flight before the sums
 #pragma unroll
       for (int i = 0; i < kDecMaxE / 32; ++i) {
         const int e = lane + 32 * i;
-        v[i] = e < E ? __ldcg(a.logits + t * E + e) : -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kDecRSlices; ++q) ps[q][i] = e < E ? __ldcg(a.logits + ((int64_t)q * T + t) * E + e) : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < kDecMaxE / 32; ++i) {
+        const int e = lane + 32 * i;
+        float l = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kDecRSlices; ++q) l += ps[q][i];  // slices in order, then the bias
+        if (e < E) {
+          l += a.bias ? a.bias[e] : 0.0f;
+          if (blockIdx.x == 0 && a.user_logits) a.user_logits[t * E + e] = l;
+        }
+        v[i] = e < E ? l : -INFINITY;
       }
       uint32_t free_mask = 0;
 #pragma unroll
@@ -446,7 +486,8 @@ __global__ void __launch_bounds__(kDecBlock, 1)
   const int ncb_r = (nbox_r + kDecGMaxBox - 1) / kDecGMaxBox, bpb_r = (nbox_r + ncb_r - 1) / ncb_r;
   const int ncb_s = nbox_s > 0 ? (nbox_s + kDecGMaxBox - 1) / kDecGMaxBox : 0;
   const int bpb_s = ncb_s > 0 ? (nbox_s + ncb_s - 1) / ncb_s : 1;
-  const int SG = 2 * (H / kDecGRows);  // steps per unit
+  const int RS = H / kDecGRows;  // 32-row slices of H
+  const int SG = 2 * RS;         // steps per unit: the gate slices, then the up slices
   const PhaseSteps phg{(int64_t)(n_routed * ncb_r + ncb_s) * SG, G};
   const int64_t gs0 = phg.start(blockIdx.x), gs1 = phg.start(blockIdx.x + 1);
   for (int c = tid; c <= G; c += kDecBlock) sh.cta_start[c] = (int)phg.start(c);
@@ -552,7 +593,7 @@ __global__ void __launch_bounds__(kDecBlock, 1)
         }
         int u, cb, nbx, bpb;
         g_unit(ii, u, cb, nbx, bpb);
-        const int r0 = (is >> 1) * kDecGRows, gu = is & 1;
+        const int gu = is >= RS ? 1 : 0, r0 = (is - gu * RS) * kDecGRows;
         const CUtensorMap* map = u < n_routed ? (gu ? &tm_up : &tm_gate) : (gu ? &tm_sup : &tm_sgate);
         const int b = j % kDecBufs;
         const int row0 = (u < n_routed ? sh.ex_id[u] * H : 0) + r0;
@@ -629,13 +670,14 @@ __global__ void __launch_bounds__(kDecBlock, 1)
   // CTA's share) the sums go to part_g (a unit streamed whole) or to piece slot 2c (the
   // CTA's first piece) or 2c + 1 (its last).
   {
-    // A fragments of one 32-row slice of H (two k16 halves): rows = the unit's tokens
+    // A fragments of one 32-row slice of H (two k16 halves) for step st of unit i: rows =
+    // the unit's tokens
     auto load_af = [&](int i, int st, uint32_t (&af)[2][4]) {
       int u, cb, nbx, bpb;
       g_unit(i, u, cb, nbx, bpb);
       int sb, ns;
       slot_rows(u, sb, ns);
-      const int g0 = lane >> 2, t4 = lane & 3, k0 = (st >> 1) * kDecGRows;
+      const int g0 = lane >> 2, t4 = lane & 3, k0 = (st >= RS ? st - RS : st) * kDecGRows;
       const __nv_bfloat16* x0 = a.x + (int64_t)slot_tok(sb + (g0 < ns ? g0 : 0)) * H;
       const __nv_bfloat16* x1 = a.x + (int64_t)slot_tok(sb + (g0 + 8 < ns ? g0 + 8 : 0)) * H;
 #pragma unroll
@@ -647,12 +689,14 @@ __global__ void __launch_bounds__(kDecBlock, 1)
         af[kq][3] = g0 + 8 < ns ? *reinterpret_cast<const uint32_t*>(x1 + kb + 8) : 0u;
       }
     };
-    float ag[kDecGMaxBox][4], au[kDecGMaxBox][4];
+    float acc[kDecGMaxBox][4];  // the gate or the up sums of the current unit
 #pragma unroll
     for (int x = 0; x < kDecGMaxBox; ++x)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) ag[x][q] = au[x][q] = 0.0f;
-    auto flush = [&](int i) {
+      for (int q = 0; q < 4; ++q) acc[x][q] = 0.0f;
+    // the sums of unit i's gate (gu 0) or up (gu 1) steps in this CTA, to part_g (whole
+    // unit) or its piece slot
+    auto flush = [&](int i, int gu) {
       int u, cb, nbx, bpb;
       g_unit(i, u, cb, nbx, bpb);
       int sb, ns;
@@ -665,52 +709,44 @@ __global__ void __launch_bounds__(kDecBlock, 1)
       for (int x = 0; x < kDecGMaxBox; ++x) {
         if (x < nbx) {
 #pragma unroll
-          for (int gu = 0; gu < 2; ++gu) {
-#pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {
-              const int r = r0 + 8 * h8;
-              if (r < ns) {
-                const float v0 = gu ? au[x][2 * h8] : ag[x][2 * h8];
-                const float v1 = gu ? au[x][2 * h8 + 1] : ag[x][2 * h8 + 1];
-                float* dst = whole ? a.part_g + ((int64_t)(sb + r) * 2 + gu) * Fm + (cb * bpb + x) * 64 + cq
-                                   : a.piece_g + (((int64_t)ps * 2 + gu) * T + r) * kDecGMaxCols + x * 64 + cq;
-                *reinterpret_cast<float2*>(dst) = make_float2(v0, v1);
-              }
+          for (int h8 = 0; h8 < 2; ++h8) {
+            const int r = r0 + 8 * h8;
+            if (r < ns) {
+              float* dst = whole ? a.part_g + ((int64_t)(sb + r) * 2 + gu) * Fm + (cb * bpb + x) * 64 + cq
+                                 : a.piece_g + (((int64_t)ps * 2 + gu) * T + r) * kDecGMaxCols + x * 64 + cq;
+              *reinterpret_cast<float2*>(dst) = make_float2(acc[x][2 * h8], acc[x][2 * h8 + 1]);
             }
           }
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ag[x][q] = au[x][q] = 0.0f;
+        for (int q = 0; q < 4; ++q) acc[x][q] = 0.0f;
       }
     };
     if (nG > 0) {
       int ci = (int)(gs0 / SG), cs = (int)(gs0 - (int64_t)ci * SG);  // unit and step of the tile
-      int ai = ci, as = cs & ~1;  // the slice whose A fragments are in an
+      int ai = ci, as = cs;  // the step whose A fragments are in an
       uint32_t af[2][4], an[2][4];
       load_af(ai, as, an);
       for (int64_t g = gs0; g < gs1; ++g, ++j) {
-        if (g == gs0 || (cs & 1) == 0) {  // a new 32-row slice: its A fragments, and the next slice's in flight
+        // this step's A fragments, and the next step's in flight
 #pragma unroll
-          for (int kq = 0; kq < 2; ++kq)
+        for (int kq = 0; kq < 2; ++kq)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) af[kq][q] = an[kq][q];
-          as += 2;
-          if (as == SG) {
-            as = 0;
-            ++ai;
-          }
-          if ((int64_t)ai * SG + as < gs1) load_af(ai, as, an);
+          for (int q = 0; q < 4; ++q) af[kq][q] = an[kq][q];
+        if (++as == SG) {
+          as = 0;
+          ++ai;
         }
+        if (g + 1 < gs1) load_af(ai, as, an);
         if (!wait_full(sh, a, j)) break;  // the barrier below makes every warp leave
         int u, cb, nbx, bpb;
         g_unit(ci, u, cb, nbx, bpb);
         const uint32_t wt = smem_u32(tiles + (j % kDecBufs) * kDecTileBytes);
-        if (cs & 1)
-          step_mma_rows(wt, nbx, af, au);
-        else
-          step_mma_rows(wt, nbx, af, ag);
-        release(sh, j);
-        if (g + 1 == gs1 || cs + 1 == SG) flush(ci);
+        uint32_t bf[2][kDecGMaxBox][2];
+        step_load_rows(wt, nbx, bf);
+        release(sh, j);  // the tile is in registers: its buffer can be refilled meanwhile
+        step_mma_rows(nbx, af, bf, acc);
+        if (g + 1 == gs1 || cs + 1 == RS || cs + 1 == SG) flush(ci, cs >= RS ? 1 : 0);
         if (++cs == SG) {
           cs = 0;
           ++ci;
@@ -752,8 +788,8 @@ __global__ void __launch_bounds__(kDecBlock, 1)
         const int bpb = u < n_routed ? bpb_r : bpb_s;
         const int cb = (f >> 6) / bpb;
         const int i = (u < n_routed ? u * ncb_r : n_routed * ncb_r) + cb;
-        const int ub = i * SG;
-        const int clo = pht.cta_of((uint32_t)ub), chi = pht.cta_of((uint32_t)(ub + SG - 1));
+        const int ub = i * SG, um = ub + RS, ue = ub + SG;  // gate steps [ub, um), up steps [um, ue)
+        const int clo = pht.cta_of((uint32_t)ub), chi = pht.cta_of((uint32_t)(ue - 1));
         if (clo == chi) {
           if (sub == 0) {
             const float* pg = a.part_g + (int64_t)sl[b2] * 2 * Fm + f;
@@ -767,16 +803,19 @@ __global__ void __launch_bounds__(kDecBlock, 1)
             const int q = clo + sub + 8 * m;
             if (q <= chi && pht.start[q] < pht.start[q + 1]) {
               const int ps = (q > clo || pht.start[clo] == ub) ? 2 * q : 2 * q + 1;
+              const int lo = max(ub, pht.start[q]), hi = min(ue, pht.start[q + 1]);  // the piece's steps
               const float* pp = a.piece_g + ((int64_t)ps * 2 * T + row) * kDecGMaxCols + colp;
-              pgv[b2][m] = __ldcg(reinterpret_cast<const float4*>(pp));
-              puv[b2][m] = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)T * kDecGMaxCols));
+              if (lo < um) pgv[b2][m] = __ldcg(reinterpret_cast<const float4*>(pp));
+              if (hi > um) puv[b2][m] = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)T * kDecGMaxCols));
             }
           }
           for (int q0 = clo + sub + 32; q0 <= chi; q0 += 8) {  // more than 32 pieces
             if (pht.start[q0] < pht.start[q0 + 1]) {
+              const int lo = max(ub, pht.start[q0]), hi = min(ue, pht.start[q0 + 1]);
               const float* pp = a.piece_g + ((int64_t)2 * q0 * 2 * T + row) * kDecGMaxCols + colp;
-              const float4 g4 = __ldcg(reinterpret_cast<const float4*>(pp));
-              const float4 u4 = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)T * kDecGMaxCols));
+              const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+              const float4 g4 = lo < um ? __ldcg(reinterpret_cast<const float4*>(pp)) : z4;
+              const float4 u4 = hi > um ? __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)T * kDecGMaxCols)) : z4;
               pgv[b2][3].x += g4.x; pgv[b2][3].y += g4.y; pgv[b2][3].z += g4.z; pgv[b2][3].w += g4.w;
               puv[b2][3].x += u4.x; puv[b2][3].y += u4.y; puv[b2][3].z += u4.z; puv[b2][3].w += u4.w;
             }
@@ -825,8 +864,11 @@ __global__ void __launch_bounds__(kDecBlock, 1)
       if (!wait_full(sh, a, j)) break;  // the barrier below makes every warp leave
       const int i = d_unit(cc), u = i / nhb;
       const uint32_t wt = smem_u32(tiles + (j % kDecBufs) * kDecTileBytes);
-      step_mma_down(wt, min(kDecStepRows, fu(u) - cc.fk * kDecStepRows), d0, d1);
-      release(sh, j);
+      const int nrows = min(kDecStepRows, fu(u) - cc.fk * kDecStepRows);
+      uint32_t fa[16][4], fb[16][2];
+      step_load_down(wt, nrows, fa, fb);
+      release(sh, j);  // the tile is in registers: its buffer can be refilled meanwhile
+      step_mma_down(nrows, fa, fb, d0, d1);
       if (cc.fk + 1 == kc2(u)) {  // the unit's last step: its y rows
         const int hb = i % nhb;
         int sb, ns;
@@ -909,7 +951,7 @@ static int64_t dec_slots(int64_t T, int64_t k) { return T * k + T; }
 size_t decode_scratch_bytes(int64_t T, int64_t H, int64_t F, int64_t E, int64_t k, int64_t Fs) {
   const int64_t Fm = F > Fs ? F : Fs, S = dec_slots(T, k);
   auto up = [](int64_t n) { return (size_t)((n + 255) / 256 * 256); };
-  return up(T * E * 4) + up(S * Fm * 2) + up(S * H * 4) + up(S * 2 * Fm * 4) +
+  return up(kDecRSlices * T * E * 4) + up(S * Fm * 2) + up(S * H * 4) + up(S * 2 * Fm * 4) +
          up((int64_t)2 * kDecMaxGrid * 2 * T * kDecGMaxCols * 4) + 256;
 }
 
@@ -938,7 +980,7 @@ cudaError_t launch_decode_fwd(int T, int H, int F, int E, int k, int Fs, const v
   a.user_w = user_w;
   a.user_logits = user_logits;
   a.logits = reinterpret_cast<float*>(b);
-  b += up((int64_t)T * E * 4);
+  b += up((int64_t)kDecRSlices * T * E * 4);
   a.hbuf = reinterpret_cast<__nv_bfloat16*>(b);
   b += up(S * Fm * 2);
   a.ypair = reinterpret_cast<float*>(b);
