@@ -79,7 +79,7 @@ struct DecodeArgs {
   float* ypair;       // [slots][H]
   float* part_g;      // [slots][gate, up][Fm]: x Wg and x Wu of a unit streamed by one CTA
   float* piece_g;     // [2 * kDecMaxGrid][gate, up][T][kDecGMaxCols]: pieces of split units
-  unsigned* sync;     // grid barrier counter (zeroed before the launch)
+  unsigned* sync;     // grid barrier counter (zeroed by the caller before the launch)
   int* status;
 };
 
@@ -964,7 +964,7 @@ cudaError_t launch_decode_fwd(int T, int H, int F, int E, int k, int Fs, const v
                               const float* bias, const void* w_gate, const void* w_up, const void* w_down,
                               const void* ws_gate, const void* ws_up, const void* ws_down, void* y, int* topk_idx,
                               float* topk_w, int* user_idx, float* user_w, float* user_logits, void* scratch,
-                              int* status, int num_sms, cudaStream_t st) {
+                              int* status, unsigned* sync, int num_sms, cudaStream_t st) {
   const int64_t Fm = F > Fs ? F : Fs, S = dec_slots(T, k);
   auto up = [](int64_t n) { return (int64_t)((n + 255) / 256 * 256); };
   char* b = static_cast<char*>(scratch);
@@ -989,10 +989,9 @@ cudaError_t launch_decode_fwd(int T, int H, int F, int E, int k, int Fs, const v
   b += up(S * 2 * Fm * 4);
   a.piece_g = reinterpret_cast<float*>(b);
   b += up((int64_t)2 * kDecMaxGrid * 2 * T * kDecGMaxCols * 4);
-  a.sync = reinterpret_cast<unsigned*>(b);
   a.status = status;
-  cudaError_t e = cudaMemsetAsync(a.sync, 0, sizeof(unsigned), st);
-  if (e != cudaSuccess) return e;
+  a.sync = sync;  // zeroed by the caller on the same stream
+  cudaError_t e = cudaSuccess;
   CUtensorMap mg, mu, md, msg, msu, msd, mh;
   bool ok = dec_map(&mg, w_gate, (int64_t)E * H, F, kDecGRows) && dec_map(&mu, w_up, (int64_t)E * H, F, kDecGRows) &&
             dec_map(&md, w_down, (int64_t)E * F, H, kDecBoxRows);

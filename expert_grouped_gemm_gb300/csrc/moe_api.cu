@@ -101,7 +101,7 @@ WsLayout make_layout(const moe_dims* d) {
     L.part_elems = per * kMaxSplit;
   }
   const int64_t sizes[] = {
-      256,                       // status
+      256,                       // status (the decode kernel's barrier counter at byte 16)
       T * E * 4,                 // logits
       T * k * 4, T * k * 4,      // topk idx, w
       T * 4,                     // xnorm
@@ -699,11 +699,14 @@ int moe_fwd_decode(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const WsPtrs p = make_ptrs(L, ws);
-  CK(cudaMemsetAsync(p.status, 0, sizeof(int), st));
+  // one memset for the status word and, 16 bytes further in the same 256-byte entry,
+  // the decode kernel's grid-barrier counter
+  unsigned* dec_sync = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(p.status) + 16);
+  CK(cudaMemsetAsync(p.status, 0, 32, st));
   g_launches += 1;
   CK(launch_decode_fwd((int)L.T, (int)L.H, (int)L.F, (int)L.E, (int)L.k, (int)L.Fs, x, w_router, router_bias, w_gate,
                        w_up, w_down, ws_gate, ws_up, ws_down, y, p.topk_idx, p.topk_w, topk_idx, topk_w, logits,
-                       p.decode, p.status, num_sms_current(), st));
+                       p.decode, p.status, dec_sync, num_sms_current(), st));
   // inference only: the routing buffers no longer hold a forward the backward could use
   std::lock_guard<std::mutex> lk(g_mu);
   g_state[ws] = State();
