@@ -31,7 +31,8 @@ MOE_RECOMPUTE = 2
 
 EXPORTED = ["moe_workspace_size", "moe_fwd", "moe_select_retained", "moe_bwd", "moe_read_status",
             "moe_last_error", "moe_workspace_entry", "moe_kernel_launches", "moe_timing_enable",
-            "moe_timing_read", "moe_route_noalloc", "moe_plan_quota", "moe_selftest_wait", "moe_fwd_decode"]
+            "moe_timing_read", "moe_route_noalloc", "moe_plan_quota", "moe_selftest_wait", "moe_fwd_decode",
+            "moe_selftest_decode_wait"]
 
 
 class MoeError(RuntimeError):
@@ -63,6 +64,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.moe_workspace_size.argtypes = [D, ctypes.POINTER(ctypes.c_size_t)]
     lib.moe_fwd.argtypes = [D, vp, ctypes.c_size_t, vp] + [vp] * 10 + [i32p, f32p, i32p, i32p, f32p]
     lib.moe_fwd_decode.argtypes = [D, vp, ctypes.c_size_t, vp] + [vp] * 10 + [i32p, f32p, f32p]
+    lib.moe_selftest_decode_wait.argtypes = [D, vp, ctypes.c_size_t, vp] + [vp] * 10 + [ctypes.c_int, ctypes.c_int64]
     lib.moe_select_retained.argtypes = [D, vp, ctypes.c_size_t, vp, vp, i32p, i32p, i32p, f32p]
     lib.moe_bwd.argtypes = [D, vp, ctypes.c_size_t, vp, vp, vp, ctypes.c_int] + [vp] * 8
     lib.moe_read_status.argtypes = [vp, vp]
@@ -79,7 +81,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.moe_kernel_launches.restype = ctypes.c_int64
     lib.moe_timing_enable.argtypes = [ctypes.c_int]
     lib.moe_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]
-    for name in ["moe_workspace_size", "moe_fwd", "moe_fwd_decode", "moe_select_retained", "moe_bwd", "moe_read_status",
+    for name in ["moe_workspace_size", "moe_fwd", "moe_fwd_decode", "moe_selftest_decode_wait", "moe_select_retained",
+                 "moe_bwd", "moe_read_status",
                  "moe_workspace_entry", "moe_timing_enable", "moe_timing_read"]:
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -159,6 +162,20 @@ def moe_fwd_decode(dims: Dims, ws: torch.Tensor, x, w_router, router_bias, w_gat
         _ptr(ws_gate, "ws_gate", io, False), _ptr(ws_up, "ws_up", io, False), _ptr(ws_down, "ws_down", io, False),
         _ptr(y, "y", io), _ptr(topk_idx, "topk_idx", torch.int32, False), _ptr(topk_w, "topk_w", torch.float32, False),
         _ptr(logits, "logits", torch.float32, False))
+    _check(rc)
+
+
+def moe_selftest_decode_wait(dims: Dims, ws: torch.Tensor, x, w_router, router_bias, w_gate, w_up, w_down, ws_gate,
+                             ws_up, ws_down, y, barrier: int, limit_us: int, stream=None):
+    """moe_fwd_decode with grid barrier `barrier` (1..4) unreachable and every wait bounded
+    by limit_us: the workspace status word becomes MOE_ERR_TIMEOUT."""
+    io = _io_dtype(dims)
+    rc = load().moe_selftest_decode_wait(
+        ctypes.byref(dims), _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream),
+        _ptr(x, "x", io), _ptr(w_router, "w_router", io), _ptr(router_bias, "router_bias", torch.float32, False),
+        _ptr(w_gate, "w_gate", io), _ptr(w_up, "w_up", io), _ptr(w_down, "w_down", io),
+        _ptr(ws_gate, "ws_gate", io, False), _ptr(ws_up, "ws_up", io, False), _ptr(ws_down, "ws_down", io, False),
+        _ptr(y, "y", io), int(barrier), int(limit_us))
     _check(rc)
 
 

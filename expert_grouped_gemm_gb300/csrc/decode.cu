@@ -81,6 +81,8 @@ struct DecodeArgs {
   float* piece_g;     // [2 * kDecMaxGrid][gate, up][T][kDecGMaxCols]: pieces of split units
   unsigned* sync;     // grid barrier counter (zeroed by the caller before the launch)
   int* status;
+  uint64_t wait_ns;   // limit of every wait (1 s; shorter in the self-test)
+  unsigned stall;     // self-test: grid barrier number that needs one arrival more than the grid has (0: none)
 };
 
 struct DecodeShared {
@@ -169,11 +171,11 @@ __device__ __forceinline__ void dec_grid_arrive(const DecodeArgs& a, DecodeShare
 template <bool kAll>
 __device__ bool dec_grid_wait(const DecodeArgs& a, DecodeShared& sh, unsigned phase) {
   if (threadIdx.x == 0 && !sh.abort_flag) {
-    const unsigned target = phase * gridDim.x;
+    const unsigned target = phase * gridDim.x + (phase == a.stall ? 1u : 0u);
     if (ld_acquire_gpu(a.sync) < target) {
       const uint64_t t0 = globaltimer_ns();
       while (ld_acquire_gpu(a.sync) < target) {
-        if (globaltimer_ns() - t0 > kDecWaitNs) {
+        if (globaltimer_ns() - t0 > a.wait_ns) {
           sh.abort_flag = 1;
           set_status(a.status, MOE_ERR_TIMEOUT);
           break;
@@ -204,7 +206,7 @@ struct PhaseTable {
 // wait ran out or another role gave up.
 __device__ __forceinline__ bool wait_full(DecodeShared& sh, const DecodeArgs& a, int j) {
   const int b = j % kDecBufs;
-  if (mbar_wait_bounded(&sh.full[b], (uint32_t)((j / kDecBufs) & 1), (volatile int*)&sh.abort_flag, kDecWaitNs))
+  if (mbar_wait_bounded(&sh.full[b], (uint32_t)((j / kDecBufs) & 1), (volatile int*)&sh.abort_flag, a.wait_ns))
     return true;
   set_status(a.status, MOE_ERR_TIMEOUT);
   return false;
@@ -574,7 +576,7 @@ __global__ void __launch_bounds__(kDecBlock, 1)
           const uint64_t now = globaltimer_ns();
           if (t0 == 0)
             t0 = now;
-          else if (now - t0 > kDecWaitNs) {
+          else if (now - t0 > a.wait_ns) {
             sh.abort_flag = 1;
             set_status(a.status, MOE_ERR_TIMEOUT);
             return false;
@@ -636,7 +638,7 @@ __global__ void __launch_bounds__(kDecBlock, 1)
             ok = false;
             break;
           }
-          if (globaltimer_ns() - t0 > kDecWaitNs) {
+          if (globaltimer_ns() - t0 > a.wait_ns) {
             sh.abort_flag = 1;
             set_status(a.status, MOE_ERR_TIMEOUT);
             ok = false;
@@ -964,7 +966,8 @@ cudaError_t launch_decode_fwd(int T, int H, int F, int E, int k, int Fs, const v
                               const float* bias, const void* w_gate, const void* w_up, const void* w_down,
                               const void* ws_gate, const void* ws_up, const void* ws_down, void* y, int* topk_idx,
                               float* topk_w, int* user_idx, float* user_w, float* user_logits, void* scratch,
-                              int* status, unsigned* sync, int num_sms, cudaStream_t st) {
+                              int* status, unsigned* sync, int num_sms, cudaStream_t st, unsigned stall,
+                              uint64_t wait_ns) {
   const int64_t Fm = F > Fs ? F : Fs, S = dec_slots(T, k);
   auto up = [](int64_t n) { return (int64_t)((n + 255) / 256 * 256); };
   char* b = static_cast<char*>(scratch);
@@ -991,6 +994,8 @@ cudaError_t launch_decode_fwd(int T, int H, int F, int E, int k, int Fs, const v
   b += up((int64_t)2 * kDecMaxGrid * 2 * T * kDecGMaxCols * 4);
   a.status = status;
   a.sync = sync;  // zeroed by the caller on the same stream
+  a.stall = stall;
+  a.wait_ns = wait_ns;
   cudaError_t e = cudaSuccess;
   CUtensorMap mg, mu, md, msg, msu, msd, mh;
   bool ok = dec_map(&mg, w_gate, (int64_t)E * H, F, kDecGRows) && dec_map(&mu, w_up, (int64_t)E * H, F, kDecGRows) &&

@@ -671,10 +671,12 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
   return MOE_OK;
 }
 
-int moe_fwd_decode(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const void* x, const void* w_router,
-                   const float* router_bias, const void* w_gate, const void* w_up, const void* w_down,
-                   const void* ws_gate, const void* ws_up, const void* ws_down, void* y, int32_t* topk_idx,
-                   float* topk_w, float* logits) {
+// moe_fwd_decode and its self-test: stall (1..4) makes that grid barrier of the kernel
+// unreachable, wait_ns bounds every wait inside it.
+static int fwd_decode_impl(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const void* x,
+                           const void* w_router, const float* router_bias, const void* w_gate, const void* w_up,
+                           const void* w_down, const void* ws_gate, const void* ws_up, const void* ws_down, void* y,
+                           int32_t* topk_idx, float* topk_w, float* logits, unsigned stall, uint64_t wait_ns) {
   WsLayout L;
   int rc = check_ws(dims, ws, ws_bytes, &L);
   if (rc) return rc;
@@ -706,11 +708,30 @@ int moe_fwd_decode(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream
   g_launches += 1;
   CK(launch_decode_fwd((int)L.T, (int)L.H, (int)L.F, (int)L.E, (int)L.k, (int)L.Fs, x, w_router, router_bias, w_gate,
                        w_up, w_down, ws_gate, ws_up, ws_down, y, p.topk_idx, p.topk_w, topk_idx, topk_w, logits,
-                       p.decode, p.status, dec_sync, num_sms_current(), st));
+                       p.decode, p.status, dec_sync, num_sms_current(), st, stall, wait_ns));
   // inference only: the routing buffers no longer hold a forward the backward could use
   std::lock_guard<std::mutex> lk(g_mu);
   g_state[ws] = State();
   return MOE_OK;
+}
+
+int moe_fwd_decode(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const void* x, const void* w_router,
+                   const float* router_bias, const void* w_gate, const void* w_up, const void* w_down,
+                   const void* ws_gate, const void* ws_up, const void* ws_down, void* y, int32_t* topk_idx,
+                   float* topk_w, float* logits) {
+  return fwd_decode_impl(dims, ws, ws_bytes, stream, x, w_router, router_bias, w_gate, w_up, w_down, ws_gate, ws_up,
+                         ws_down, y, topk_idx, topk_w, logits, 0u, 1000000000ull);
+}
+
+int moe_selftest_decode_wait(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const void* x,
+                             const void* w_router, const float* router_bias, const void* w_gate, const void* w_up,
+                             const void* w_down, const void* ws_gate, const void* ws_up, const void* ws_down,
+                             void* y, int barrier, int64_t limit_us) {
+  if (barrier < 1 || barrier > 4) return fail(MOE_ERR_INVALID_ARG, "moe_selftest_decode_wait: barrier must be 1..4");
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(MOE_ERR_INVALID_ARG, "moe_selftest_decode_wait: limit_us must be 1..1000000");
+  return fwd_decode_impl(dims, ws, ws_bytes, stream, x, w_router, router_bias, w_gate, w_up, w_down, ws_gate, ws_up,
+                         ws_down, y, nullptr, nullptr, nullptr, (unsigned)barrier, (uint64_t)limit_us * 1000ull);
 }
 
 int moe_select_retained(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const void* dy,

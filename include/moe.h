@@ -257,6 +257,23 @@ MOE_API int moe_plan_quota(const moe_dims* dims, void* ws, size_t ws_bytes, void
 MOE_API int moe_selftest_wait(void* stream, int arrive, int64_t limit_us, int32_t* device_status);
 
 /*
+ * moe_selftest_decode_wait -- checks, on the GPU, the failure path of the fused decode
+ * kernel: runs moe_fwd_decode (same arguments, same rules; no optional outputs) with
+ * grid barrier `barrier` (1 = after the router, 2 = after gate/up, 3 = after h,
+ * 4 = after down) needing one arrival more than the grid has, and every wait inside
+ * the kernel bounded by limit_us (1 .. 1,000,000) instead of 1 s. That wait runs out,
+ * the kernel writes MOE_ERR_TIMEOUT to the workspace status word (moe_read_status),
+ * every warp leaves and the kernel returns with its copies landed: the context stays
+ * usable and the next moe_fwd_decode on the workspace computes normally. y is left
+ * unspecified.
+ */
+MOE_API int moe_selftest_decode_wait(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream,
+                                     const void* x, const void* w_router, const float* router_bias,
+                                     const void* w_gate, const void* w_up, const void* w_down,
+                                     const void* ws_gate, const void* ws_up, const void* ws_down, void* y,
+                                     int barrier, int64_t limit_us);
+
+/*
  * moe_read_status -- synchronises `stream` and returns the device status word
  * of the workspace (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_ARG), then
  * clears it. Returns MOE_ERR_CUDA if the synchronisation itself failed.

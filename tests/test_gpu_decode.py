@@ -127,3 +127,32 @@ def test_decode_router_ties_go_to_the_lower_expert():
     assert np.array_equal(g["idx"], want), g["idx"]
     assert np.all(g["w"] == np.float32(0.125))
     check_decode(w, inp, g)
+
+
+@pytest.mark.parametrize("barrier", [1, 2, 3, 4])
+def test_decode_wait_that_runs_out_reports_timeout(barrier):
+    """A grid barrier that can never complete: the bounded wait runs out, the kernel reports
+    MOE_ERR_TIMEOUT and returns, and the next call on the same workspace is correct."""
+    w = custom("dec_stall", T=8, k=8, **QWEN)
+    inp = make_inputs(w, seed=13)
+    layer = MoELayer(w, inp, record_routing=True)
+    p = layer.p
+    x = inp["x"].cuda()
+    _lib.moe_selftest_decode_wait(layer.dims, layer.ws, x, p["w_router"], p["router_bias"], p["w_gate"], p["w_up"],
+                                  p["w_down"], p["ws_gate"], p["ws_up"], p["ws_down"], layer.y, barrier, 20000)
+    assert _lib.moe_read_status(layer.ws) == _lib.MOE_ERR_TIMEOUT
+    g, _ = run_decode(w, inp, layer)
+    check_decode(w, inp, g)
+
+
+def test_decode_selftest_rejects_bad_arguments():
+    w = custom("dec_stall_args", T=2, k=2, **QWEN)
+    inp = make_inputs(w, seed=1)
+    layer = MoELayer(w, inp)
+    p = layer.p
+    for barrier, limit in ((0, 1000), (5, 1000), (1, 0), (1, 2000000)):
+        with pytest.raises(_lib.MoeError) as ei:
+            _lib.moe_selftest_decode_wait(layer.dims, layer.ws, inp["x"].cuda(), p["w_router"], p["router_bias"],
+                                          p["w_gate"], p["w_up"], p["w_down"], p["ws_gate"], p["ws_up"],
+                                          p["ws_down"], layer.y, barrier, limit)
+        assert ei.value.code == _lib.MOE_ERR_INVALID_ARG
