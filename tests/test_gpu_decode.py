@@ -156,3 +156,16 @@ def test_decode_selftest_rejects_bad_arguments():
                                           p["w_gate"], p["w_up"], p["w_down"], p["ws_gate"], p["ws_up"],
                                           p["ws_down"], layer.y, barrier, limit)
         assert ei.value.code == _lib.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("shape", [
+    dict(T=5, H=256, F=192, E=48, k=3),     # E not a multiple of 32: top-k lanes past E
+    dict(T=16, H=512, F=256, E=64, k=16),   # T * k = 256 routed pairs, the most the kernel takes
+    dict(T=2, H=1024, F=1024, E=256, k=8),  # E = 256; F in two column blocks of 512
+    dict(T=3, H=320, F=1600, E=32, k=4, F_shared=832),  # F in three blocks, a shared expert in two
+])
+def test_decode_parity_edge_shapes(shape):
+    w = custom("dec_edge_" + "_".join(f"{kk}{v}" for kk, v in shape.items()), zipf_s=0.8, **shape)
+    inp = make_inputs(w, seed=17)
+    g, _ = run_decode(w, inp)
+    print(w.name, check_decode(w, inp, g))
