@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(256) k_pair_score(const TIO* dy, const TIO* y_
                                                     const int* pad_total, const float* topk_w, const float* xnorm,
                                                     int H, int k, float* g, float* score, TIO* dy_perm,
                                                     float* user_scores) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const int nrows = *pad_total;
   const int lane = threadIdx.x & 31;
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < nrows; r += (gridDim.x * blockDim.x) >> 5) {
@@ -106,6 +107,7 @@ constexpr int kSelCache = 8192;  // keys of an expert kept in shared memory (row
 __global__ void __launch_bounds__(kSelThreads) k_select(const float* score, const int* count, const int* pad_off,
                                                         const int* quota, int* ret_cidx, int* ret_count,
                                                         int* status) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   __shared__ uint32_t s_key[kSelCache];
   __shared__ int hist[256];
   __shared__ int wtot[kSelThreads / 32];
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(1024) k_ret_scan(const int* ret_count, int E, 
                                                    int* ret_tile_off, int* ret_src, int* user_offsets, int* order,
                                                    int* ret_tile_off2, int4* tile_rec, int4* ord_rec,
                                                    int4* tile_rec2) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const int e = threadIdx.x;
   const int cnt = e < E ? ret_count[e] : 0;
   const int rank = order ? block_order_desc(cnt, E, order) : 0;
@@ -228,6 +231,7 @@ __global__ void __launch_bounds__(1024) k_ret_scan(const int* ret_count, int E, 
 __global__ void k_ret_index(const int* topk_idx, const int* rowp_of_pair, const int* row_of_pair,
                             const int* ret_cidx, const int* ret_offset, const int* ret_pad_off, int64_t P,
                             int* ret_src, int* crow_of_pair, int* ret_rows, int* user_rows) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   for (int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; p < P; p += (int64_t)gridDim.x * blockDim.x) {
     const int r = rowp_of_pair[p];
     const int c = ret_cidx[r];
@@ -261,6 +265,7 @@ __global__ void __launch_bounds__(256) k_compact_rows(const int* ret_src, const 
                                                       const int* pair_of_row, const float* topk_w, const TIO* x,
                                                       const TIO* ab, const TIO* h, const TIO* dy, int H, int F, int k,
                                                       TIO* x_c, TIO* ab_c, TIO* h_c, TIO* dy_c) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const int nrows = *ret_pad_total;
   const int lane = threadIdx.x & 31;
   for (int c = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; c < nrows; c += (gridDim.x * blockDim.x) >> 5) {
@@ -326,6 +331,7 @@ template <typename TIO>
 __global__ void __launch_bounds__(256) k_router_bwd(const float* g, const int* rowp_of_pair, const int* topk_idx,
                                                     const float* topk_w, int T, int Tpad, int E, int k,
                                                     float* dl_sel, TIO* dl_dense) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const int lane = threadIdx.x & 31;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tpad; t += (gridDim.x * blockDim.x) >> 5) {
     if (t >= T) {
@@ -352,6 +358,7 @@ __global__ void __launch_bounds__(256) k_router_bwd(const float* g, const int* r
 // 32x32 tiled transpose: out[c][r] = in[r][c], in is [R, Cc].
 template <typename TIO>
 __global__ void k_transpose(const TIO* in, int R, int Cc, TIO* out) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   __shared__ TIO tile[32][33];
   const int bx = blockIdx.x * 32, by = blockIdx.y * 32;
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
@@ -374,6 +381,7 @@ __global__ void __launch_bounds__(256) k_dx_reduce(const TIO* __restrict__ dx_pa
                                                    const int* __restrict__ topk_idx, const float* __restrict__ dl_sel,
                                                    const TIO* __restrict__ wrT, const TIO* __restrict__ sh_dx, int T,
                                                    int H, int k, TIO* __restrict__ dx) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   if constexpr (sizeof(TIO) == 2) {
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
       const int64_t p0 = (int64_t)t * k;
@@ -442,6 +450,7 @@ __global__ void __launch_bounds__(256) k_dx_reduce(const TIO* __restrict__ dx_pa
 // quota[e] = min(count[e], ceil(rho_num/rho_den * T*k/E)) (and <= budget[e] if given).
 __global__ void k_plan_quota(const int* count, int E, int64_t pairs, int64_t rho_num, int64_t rho_den,
                              const int* budget, int* quota) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= E) return;
   const int64_t den = rho_den * E;
@@ -454,7 +463,7 @@ __global__ void k_plan_quota(const int* count, int E, int64_t pairs, int64_t rho
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_plan_quota(const int* count, int E, int64_t pairs, int64_t rho_num, int64_t rho_den,
                               const int* budget, int* quota, cudaStream_t st) {
-  k_plan_quota<<<(E + 255) / 256, 256, 0, st>>>(count, E, pairs, rho_num, rho_den, budget, quota);
+  MOE_LAUNCH(k_plan_quota, (E + 255) / 256, 256, 0, st, count, E, pairs, rho_num, rho_den, budget, quota);
   return cudaGetLastError();
 }
 
@@ -467,22 +476,21 @@ template <typename TIO>
 cudaError_t launch_pair_score(const void* dy, const void* y_pair, const int* pair_of_row, const int* pad_total,
                               int64_t Rmax, const float* topk_w, const float* xnorm, int H, int k, float* g,
                               float* score, void* dy_perm, float* user_scores, int num_sms, cudaStream_t st) {
-  k_pair_score<TIO><<<grid_for(Rmax, num_sms), 256, 0, st>>>(
-      reinterpret_cast<const TIO*>(dy), reinterpret_cast<const TIO*>(y_pair), pair_of_row, pad_total, topk_w, xnorm,
+  MOE_LAUNCH(k_pair_score<TIO>, grid_for(Rmax, num_sms), 256, 0, st, reinterpret_cast<const TIO*>(dy), reinterpret_cast<const TIO*>(y_pair), pair_of_row, pad_total, topk_w, xnorm,
       H, k, g, score, reinterpret_cast<TIO*>(dy_perm), user_scores);
   return cudaGetLastError();
 }
 
 cudaError_t launch_select(const float* score, const int* count, const int* pad_off, const int* quota, int E,
                           int* ret_cidx, int* ret_count, int* status, cudaStream_t st) {
-  k_select<<<E, kSelThreads, 0, st>>>(score, count, pad_off, quota, ret_cidx, ret_count, status);
+  MOE_LAUNCH(k_select, E, kSelThreads, 0, st, score, count, pad_off, quota, ret_cidx, ret_count, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_ret_scan(const int* ret_count, int E, int* ret_offset, int* ret_pad_off, int* ret_tile_off,
                             int* ret_src, int* user_offsets, cudaStream_t st, int* order, int* ret_tile_off2,
                             int4* tile_rec, int4* ord_rec, int4* tile_rec2) {
-  k_ret_scan<<<1, 1024, 0, st>>>(ret_count, E, ret_offset, ret_pad_off, ret_tile_off, ret_src, user_offsets, order,
+  MOE_LAUNCH(k_ret_scan, 1, 1024, 0, st, ret_count, E, ret_offset, ret_pad_off, ret_tile_off, ret_src, user_offsets, order,
                                  ret_tile_off2, tile_rec, ord_rec, tile_rec2);
   return cudaGetLastError();
 }
@@ -492,7 +500,7 @@ cudaError_t launch_ret_index(const int* topk_idx, const int* rowp_of_pair, const
                              int* ret_src, int* crow_of_pair, int* ret_rows, int* user_rows, int num_sms,
                              cudaStream_t st) {
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((P + 255) / 256, (int64_t)num_sms * 8));
-  k_ret_index<<<grid, 256, 0, st>>>(topk_idx, rowp_of_pair, row_of_pair, ret_cidx, ret_offset, ret_pad_off, P,
+  MOE_LAUNCH(k_ret_index, grid, 256, 0, st, topk_idx, rowp_of_pair, row_of_pair, ret_cidx, ret_offset, ret_pad_off, P,
                                     ret_src, crow_of_pair, ret_rows, user_rows);
   return cudaGetLastError();
 }
@@ -502,8 +510,7 @@ cudaError_t launch_compact_rows(const int* ret_src, const int* ret_pad_total, in
                                 const float* topk_w, const void* x, const void* ab, const void* h, const void* dy,
                                 int H, int F, int k, void* x_c, void* ab_c, void* h_c, void* dy_c, int num_sms,
                                 cudaStream_t st) {
-  k_compact_rows<TIO><<<grid_for(Rmax, num_sms), 256, 0, st>>>(
-      ret_src, ret_pad_total, pair_of_row, topk_w, reinterpret_cast<const TIO*>(x), reinterpret_cast<const TIO*>(ab),
+  MOE_LAUNCH(k_compact_rows<TIO>, grid_for(Rmax, num_sms), 256, 0, st, ret_src, ret_pad_total, pair_of_row, topk_w, reinterpret_cast<const TIO*>(x), reinterpret_cast<const TIO*>(ab),
       reinterpret_cast<const TIO*>(h), reinterpret_cast<const TIO*>(dy), H, F, k, reinterpret_cast<TIO*>(x_c),
       reinterpret_cast<TIO*>(ab_c), reinterpret_cast<TIO*>(h_c), reinterpret_cast<TIO*>(dy_c));
   return cudaGetLastError();
@@ -513,7 +520,7 @@ template <typename TIO>
 cudaError_t launch_router_bwd(const float* g, const int* rowp_of_pair, const int* topk_idx, const float* topk_w,
                               int T, int Tpad, int E, int k, float* dl_sel, void* dl_dense, int num_sms,
                               cudaStream_t st) {
-  k_router_bwd<TIO><<<grid_for(Tpad, num_sms), 256, 0, st>>>(g, rowp_of_pair, topk_idx, topk_w, T, Tpad, E, k,
+  MOE_LAUNCH(k_router_bwd<TIO>, grid_for(Tpad, num_sms), 256, 0, st, g, rowp_of_pair, topk_idx, topk_w, T, Tpad, E, k,
                                                              dl_sel, reinterpret_cast<TIO*>(dl_dense));
   return cudaGetLastError();
 }
@@ -521,7 +528,7 @@ cudaError_t launch_router_bwd(const float* g, const int* rowp_of_pair, const int
 template <typename TIO>
 cudaError_t launch_transpose(const void* in, int R, int Cc, void* out, cudaStream_t st) {
   dim3 grid((Cc + 31) / 32, (R + 31) / 32), block(32, 8);
-  k_transpose<TIO><<<grid, block, 0, st>>>(reinterpret_cast<const TIO*>(in), R, Cc, reinterpret_cast<TIO*>(out));
+  MOE_LAUNCH(k_transpose<TIO>, grid, block, 0, st, reinterpret_cast<const TIO*>(in), R, Cc, reinterpret_cast<TIO*>(out));
   return cudaGetLastError();
 }
 
@@ -537,6 +544,7 @@ __global__ void __launch_bounds__(256) k_dx_reduce_k8(const __nv_bfloat16* __res
                                                       const __nv_bfloat16* __restrict__ wrT,
                                                       const __nv_bfloat16* __restrict__ sh_dx, int T, int H, int k,
                                                       __nv_bfloat16* __restrict__ dx) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const int lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
   const int nv = H / 8;
   for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
@@ -605,7 +613,7 @@ cudaError_t launch_dx_reduce(const void* dx_pair, const int* crow_of_pair, const
     const int wpb = kThreads / 32;
     const int g =
         (int)std::max<int64_t>(1, std::min<int64_t>(((int64_t)T + wpb - 1) / wpb, (int64_t)num_sms * per_sm));
-    k_dx_reduce_k8<<<g, kThreads, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(dx_pair), crow_of_pair, topk_idx, dl_sel,
+    MOE_LAUNCH(k_dx_reduce_k8, g, kThreads, 0, st, reinterpret_cast<const __nv_bfloat16*>(dx_pair), crow_of_pair, topk_idx, dl_sel,
                                       reinterpret_cast<const __nv_bfloat16*>(wrT),
                                       reinterpret_cast<const __nv_bfloat16*>(sh_dx), T, H, k,
                                       reinterpret_cast<__nv_bfloat16*>(dx));
@@ -613,8 +621,7 @@ cudaError_t launch_dx_reduce(const void* dx_pair, const int* crow_of_pair, const
   }
   const int grid = sizeof(TIO) == 2 ? (int)std::max<int64_t>(1, std::min<int64_t>(T, (int64_t)num_sms * 32))
                                     : grid_for(T, num_sms);
-  k_dx_reduce<TIO><<<grid, 256, 0, st>>>(
-      reinterpret_cast<const TIO*>(dx_pair), crow_of_pair, topk_idx, dl_sel, reinterpret_cast<const TIO*>(wrT),
+  MOE_LAUNCH(k_dx_reduce<TIO>, grid, 256, 0, st, reinterpret_cast<const TIO*>(dx_pair), crow_of_pair, topk_idx, dl_sel, reinterpret_cast<const TIO*>(wrT),
       reinterpret_cast<const TIO*>(sh_dx), T, H, k, reinterpret_cast<TIO*>(dx));
   return cudaGetLastError();
 }

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -434,5 +436,43 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+
+// ---------------------------------------------------------------- launches that overlap
+// The library's kernels run back to back on one stream. Each is launched with
+// programmatic stream serialisation and triggers nothing itself, so the next kernel's
+// CTAs are scheduled as soon as this kernel's last CTA has exited, ahead of the
+// completion flush, and wait in pdl_wait() until that flush has made this kernel's
+// writes visible: the launch gap between two kernels is hidden, and no CTA is placed
+// beside a kernel that is still running. A kernel calls pdl_wait() before its first
+// global memory access (a prologue that touches only shared and tensor memory may come
+// first). An early griddepcontrol.launch_dependents was measured slower: the next
+// kernel's CTAs took SM slots from the one still running. pdl_wait() is a no-op in a
+// kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+#ifndef MOE_PDL
+#define MOE_PDL 1  // 0: plain stream-ordered launches
+#endif
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = MOE_PDL ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+// Launch with launch_pdl and return the launch error, if any, from the enclosing function.
+#define MOE_LAUNCH(...)                                                \
+  do {                                                                 \
+    const cudaError_t moe_launch_err_ = ::moe::launch_pdl(__VA_ARGS__); \
+    if (moe_launch_err_ != cudaSuccess) return moe_launch_err_;        \
+  } while (0)
 
 }  // namespace moe

@@ -11,6 +11,7 @@
 namespace moe {
 
 __global__ void simt_grouped_gemm_f32(const GemmArgs a) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const float* A = reinterpret_cast<const float*>(a.A);
   const float* B0 = reinterpret_cast<const float*>(a.B0);
   const float* B1 = reinterpret_cast<const float*>(a.B1 ? a.B1 : a.B0);
@@ -83,7 +84,7 @@ cudaError_t launch_simt_gemm_f32(const GemmArgs& a, cudaStream_t st) {
     grid.y = (unsigned)std::min(a.M, 65535);
     grid.z = (unsigned)a.G;
   }
-  simt_grouped_gemm_f32<<<grid, block, 0, st>>>(a);
+  MOE_LAUNCH(simt_grouped_gemm_f32, grid, block, 0, st, a);
   return cudaGetLastError();
 }
 

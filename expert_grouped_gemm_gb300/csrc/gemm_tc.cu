@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(64 + 32 * NEPI, 1)
   __syncthreads();
   if constexpr (PAIR) cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
   tc_fence_after();
+  pdl_wait();  // the set-up above touched no global memory; everything below may read the previous kernel's outputs
   const uint32_t tmem_base = *tmem_slot;
   // leader barriers as seen from this CTA (shared::cluster addresses)
   const uint32_t full0 = PAIR ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
@@ -707,8 +708,8 @@ static cudaError_t launch_cfg(const GemmArgs& a, cudaStream_t st, int num_sms) {
   }
   if (!ok) return cudaErrorInvalidValue;
   if constexpr (CTAS == 1) {
-    kern<<<num_sms, C::THREADS, C::SMEM, st>>>(mA, mB0, mB1, mO0, mO1, mO0h, mO1h, a);
-    return cudaGetLastError();
+    e = launch_pdl(kern, num_sms, C::THREADS, C::SMEM, st, mA, mB0, mB1, mO0, mO1, mO0h, mO1h, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
   } else {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];

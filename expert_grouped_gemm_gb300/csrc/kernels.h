@@ -9,17 +9,20 @@
 namespace moe {
 
 // part / nsplit / part_stride: the router GEMM's fp32 partial sums when it ran as a
-// K split (null: logits already hold the sums)
+// K split (null: logits already hold the sums). masks_clear: the caller has zeroed the
+// chunk masks. logits_out / topk_idx_out / topk_w_out: optional second copies of the
+// biased logits, indices and weights (the caller's own buffers), written by the kernel.
 cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, int k, int* topk_idx, float* topk_w,
                               uint64_t* masks, cudaStream_t st, const float* part = nullptr, int nsplit = 1,
-                              int64_t part_stride = 0);
+                              int64_t part_stride = 0, bool masks_clear = false, float* logits_out = nullptr,
+                              int* topk_idx_out = nullptr, float* topk_w_out = nullptr);
 cudaError_t launch_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset, int* pad_off,
                               int* tile_off, int* chunk_base, int* pair_of_row, int* user_offsets, cudaStream_t st,
                               int* order = nullptr, int* tile_off2 = nullptr, int4* tile_rec = nullptr,
                               int4* ord_rec = nullptr, int4* tile_rec2 = nullptr);
 cudaError_t launch_route_index(const uint64_t* masks, const int* chunk_base, const int* topk_idx, const int* offset,
                                const int* pad_off, int T, int E, int k, int* rowp_of_pair, int* row_of_pair,
-                               int* pair_of_row, cudaStream_t st);
+                               int* pair_of_row, cudaStream_t st, int* row_of_pair_out = nullptr);
 template <typename TIO>
 cudaError_t launch_gather_rows(const void* x, const int* pair_of_row, const int* pad_total, int64_t Rmax, int H, int k,
                                void* x_perm, float* xnorm, int num_sms, cudaStream_t st);

@@ -102,10 +102,11 @@ WsLayout make_layout(const moe_dims* d) {
   }
   const int64_t sizes[] = {
       256,                       // status (the decode kernel's barrier counter at byte 16)
+      C * E * 8,                 // masks (right after status: one memset clears both)
       T * E * 4,                 // logits
       T * k * 4, T * k * 4,      // topk idx, w
       T * 4,                     // xnorm
-      C * E * 8, C * E * 4,      // masks, chunk_base
+      C * E * 4,                 // chunk_base
       E * 4, (E + 1) * 4, (E + 1) * 4, (E + 1) * 4,  // count offset pad_off tile_off
       P * 4, P * 4, R * 4,       // rowp_of_pair row_of_pair pair_of_row
       R * H * es, R * 2 * F * es, R * F * es, R * H * es,  // x_perm ab h y_pair
@@ -138,7 +139,7 @@ WsLayout make_layout(const moe_dims* d) {
 
 // Names of the workspace entries, in layout order (kept in step with make_ptrs).
 const char* const kEntryNames[] = {
-    "status", "logits", "topk_idx", "topk_w", "xnorm", "masks", "chunk_base", "count", "offset", "pad_off",
+    "status", "masks", "logits", "topk_idx", "topk_w", "xnorm", "chunk_base", "count", "offset", "pad_off",
     "tile_off", "rowp_of_pair", "row_of_pair", "pair_of_row", "x_perm", "ab", "h", "y_pair", "sh_ab", "sh_h",
     "sh_y", "g", "score", "dy_perm", "ret_cidx", "ret_count", "ret_offset", "ret_pad_off", "ret_tile_off",
     "ret_src", "crow_of_pair", "ret_rows", "x_c", "ab_c", "h_c", "dy_c", "dab", "dx_pair", "dl", "dl_sel", "wrT",
@@ -151,11 +152,11 @@ WsPtrs make_ptrs(const WsLayout& L, void* ws) {
   auto nx = [&]() { return static_cast<void*>(b + L.off[i++]); };
   WsPtrs p;
   p.status = (int*)nx();
+  p.masks = (uint64_t*)nx();
   p.logits = (float*)nx();
   p.topk_idx = (int*)nx();
   p.topk_w = (float*)nx();
   p.xnorm = (float*)nx();
-  p.masks = (uint64_t*)nx();
   p.chunk_base = (int*)nx();
   p.count = (int*)nx();
   p.offset = (int*)nx();
@@ -601,7 +602,8 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
   const int sms = num_sms_current();
   const int T = (int)L.T, H = (int)L.H, F = (int)L.F, E = (int)L.E, k = (int)L.k, Fs = (int)L.Fs;
 
-  CK(cudaMemsetAsync(p.status, 0, sizeof(int), st));
+  // the status word and the routing chunk masks (the next entry) start at zero
+  CK(cudaMemsetAsync(p.status, 0, L.off[2] - L.off[0], st));
 
   // router logits = x W_r  (fp32 out; bias added by the top-k kernel)
   const int rks = moe::internal_router_ksplit(dims, sms);
@@ -631,11 +633,12 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
   {
     Span sp(st, FAM_BW);
     CKL(launch_route_topk(p.logits, router_bias, T, E, k, p.topk_idx, p.topk_w, p.masks, st,
-                          rks > 1 ? p.part : nullptr, rks, (int64_t)T * E));
+                          rks > 1 ? p.part : nullptr, rks, (int64_t)T * E, /*masks_clear=*/true, logits, topk_idx,
+                          topk_w));
     CKL(launch_route_scan(p.masks, (int)L.C, E, p.count, p.offset, p.pad_off, p.tile_off, p.chunk_base, p.pair_of_row,
                          expert_offsets, st, p.order, p.tile_off2, p.tile_rec, p.ord_rec, p.tile_rec2));
     CKL(launch_route_index(p.masks, p.chunk_base, p.topk_idx, p.offset, p.pad_off, T, E, k, p.rowp_of_pair,
-                          p.row_of_pair, p.pair_of_row, st));
+                          p.row_of_pair, p.pair_of_row, st, row_of_pair));
     if (bf)
       CKL(launch_gather_rows<__nv_bfloat16>(x, p.pair_of_row, p.pad_off + E, L.Rmax, H, k, p.x_perm, p.xnorm, sms, st));
     else
@@ -650,10 +653,6 @@ int moe_fwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     else
       CKL(launch_combine<float>(p.y_pair, p.rowp_of_pair, p.topk_w, shared ? p.sh_y : nullptr, T, H, k, y, sms, st));
   }
-  if (topk_idx) CK(cudaMemcpyAsync(topk_idx, p.topk_idx, L.T * L.k * 4, cudaMemcpyDeviceToDevice, st));
-  if (topk_w) CK(cudaMemcpyAsync(topk_w, p.topk_w, L.T * L.k * 4, cudaMemcpyDeviceToDevice, st));
-  if (row_of_pair) CK(cudaMemcpyAsync(row_of_pair, p.row_of_pair, L.P * 4, cudaMemcpyDeviceToDevice, st));
-  if (logits) CK(cudaMemcpyAsync(logits, p.logits, L.T * L.E * 4, cudaMemcpyDeviceToDevice, st));
 
   std::lock_guard<std::mutex> lk(g_mu);
   State& s = g_state[ws];

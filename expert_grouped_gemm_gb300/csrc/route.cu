@@ -20,11 +20,15 @@ constexpr int kChunk = 64;  // tokens per routing chunk (one bit each in a uint6
 
 // ------------------------------------------------------------------ top-k
 // Warp per token (8 per block); lane l holds logits e = l + 32 i (i < EPL) in
-// registers. The chunk masks (zeroed by the launcher) get one bit per pair.
+// registers. The chunk masks (zeroed beforehand) get one bit per pair. ulogits,
+// uidx, uw (each may be null) receive a second copy of what goes to logits,
+// topk_idx and topk_w.
 template <int EPL>
 __global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* bias, int T, int E, int k,
                                                     int* topk_idx, float* topk_w, uint64_t* masks,
-                                                    const float* part, int nsplit, int64_t part_stride) {
+                                                    const float* part, int nsplit, int64_t part_stride,
+                                                    float* ulogits, int* uidx, float* uw) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -62,6 +66,7 @@ __global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* 
     if (e < E) {
       const float x = l[i] + (bias ? bias[e] : 0.0f);
       lrow[e] = x;                     // the biased logits the selection used
+      if (ulogits) ulogits[(int64_t)t * E + e] = x;
       v[i] = (x != x) ? -INFINITY : x;  // NaN ranks last
     }
   }
@@ -107,8 +112,12 @@ __global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* 
       }
     }
     if (lane < k) {
-      topk_idx[(int64_t)t * k + lane] = my_e;
-      topk_w[(int64_t)t * k + lane] = my_w * (1.0f / sum);
+      const int64_t q = (int64_t)t * k + lane;
+      const float w = my_w * (1.0f / sum);
+      topk_idx[q] = my_e;
+      topk_w[q] = w;
+      if (uidx) uidx[q] = my_e;
+      if (uw) uw[q] = w;
       atomicOr(reinterpret_cast<unsigned long long*>(&cmask[my_e]), bit);
     }
     return;
@@ -140,12 +149,17 @@ __global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* 
       sum += ex;
       topk_idx[(int64_t)t * k + j] = be;
       topk_w[(int64_t)t * k + j] = ex;
+      if (uidx) uidx[(int64_t)t * k + j] = be;
       atomicOr(reinterpret_cast<unsigned long long*>(&cmask[be]), bit);
     }
   }
   if (lane == 0) {
     const float inv = 1.0f / sum;
-    for (int j = 0; j < k; ++j) topk_w[(int64_t)t * k + j] *= inv;
+    for (int j = 0; j < k; ++j) {
+      const float w = topk_w[(int64_t)t * k + j] * inv;
+      topk_w[(int64_t)t * k + j] = w;
+      if (uw) uw[(int64_t)t * k + j] = w;
+    }
   }
 }
 
@@ -156,6 +170,7 @@ __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int 
                                                      int* pad_off, int* tile_off, int* chunk_base, int* pair_of_row,
                                                      int* user_offsets, int* order, int* tile_off2,
                                                      int4* tile_rec, int4* ord_rec, int4* tile_rec2) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   __shared__ int part_cnt[1024];
   int parts = 1;
   while (parts * 2 * E <= 1024) parts *= 2;
@@ -220,7 +235,9 @@ __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int 
 // grid = C chunks, block = 256.
 __global__ void __launch_bounds__(256) k_route_index(const uint64_t* masks, const int* chunk_base, const int* topk_idx,
                                                      const int* offset, const int* pad_off, int T, int E, int k,
-                                                     int* rowp_of_pair, int* row_of_pair, int* pair_of_row) {
+                                                     int* rowp_of_pair, int* row_of_pair, int* pair_of_row,
+                                                     int* urow) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   extern __shared__ uint64_t sm[];  // masks[E] then bases[E]
   int* sbase = reinterpret_cast<int*>(sm + E);
   const int c = blockIdx.x;
@@ -238,7 +255,9 @@ __global__ void __launch_bounds__(256) k_route_index(const uint64_t* masks, cons
     const int rank = __popcll(sm[e] & ((1ull << tl) - 1ull));
     const int prow = sbase[e] + rank;
     rowp_of_pair[p] = prow;
-    row_of_pair[p] = offset[e] + (prow - pad_off[e]);
+    const int r = offset[e] + (prow - pad_off[e]);
+    row_of_pair[p] = r;
+    if (urow) urow[p] = r;  // the caller's copy, when asked for
     pair_of_row[prow] = (int)p;
   }
 }
@@ -249,6 +268,7 @@ __global__ void __launch_bounds__(256) k_route_index(const uint64_t* masks, cons
 template <typename TIO>
 __global__ void __launch_bounds__(256) k_gather_rows(const TIO* x, const int* pair_of_row, const int* pad_total,
                                                      int H, int k, TIO* x_perm, float* xnorm) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const int nrows = *pad_total;
   const int lane = threadIdx.x & 31;
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < nrows; r += (gridDim.x * blockDim.x) >> 5) {
@@ -305,6 +325,7 @@ template <typename TIO>
 __global__ void __launch_bounds__(256) k_combine(const TIO* __restrict__ y_pair, const int* __restrict__ rowp_of_pair,
                                                  const float* __restrict__ topk_w, const TIO* __restrict__ sh_y, int T,
                                                  int H, int k, TIO* __restrict__ y) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   if constexpr (sizeof(TIO) == 2) {
     const int nv = H / 8;
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
@@ -360,6 +381,7 @@ __global__ void __launch_bounds__(256, 4) k_combine_k8(const __nv_bfloat16* __re
                                                     const int* __restrict__ rowp_of_pair, const float* __restrict__ topk_w,
                                                     const __nv_bfloat16* __restrict__ sh_y, int T, int H, int k,
                                                     __nv_bfloat16* __restrict__ y) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   __shared__ int s_row[2][8];
   __shared__ float s_w[2][8];
   const int tid = threadIdx.x, nv = H / 8;
@@ -412,36 +434,45 @@ __global__ void __launch_bounds__(256, 4) k_combine_k8(const __nv_bfloat16* __re
 
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_route_topk(float* logits, const float* bias, int T, int E, int k, int* topk_idx, float* topk_w,
-                              uint64_t* masks, cudaStream_t st, const float* part, int nsplit, int64_t part_stride) {
-  const int C = (T + kChunk - 1) / kChunk;
-  cudaError_t e = cudaMemsetAsync(masks, 0, (size_t)C * E * sizeof(uint64_t), st);
-  if (e != cudaSuccess) return e;
+                              uint64_t* masks, cudaStream_t st, const float* part, int nsplit, int64_t part_stride,
+                              bool masks_clear, float* logits_out, int* topk_idx_out, float* topk_w_out) {
+  if (!masks_clear) {
+    const int C = (T + kChunk - 1) / kChunk;
+    const cudaError_t e = cudaMemsetAsync(masks, 0, (size_t)C * E * sizeof(uint64_t), st);
+    if (e != cudaSuccess) return e;
+  }
   const int grid = (T + 7) / 8;
   const int epl = (E + 31) / 32;
-  if (epl <= 1) k_route_topk<1><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride);
-  else if (epl <= 2) k_route_topk<2><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride);
-  else if (epl <= 4) k_route_topk<4><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride);
-  else if (epl <= 8) k_route_topk<8><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride);
-  else if (epl <= 16) k_route_topk<16><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride);
-  else k_route_topk<32><<<grid, 256, 0, st>>>(logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride);
+  if (epl <= 1) MOE_LAUNCH(k_route_topk<1>, grid, 256, 0, st, logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride,
+                                 logits_out, topk_idx_out, topk_w_out);
+  else if (epl <= 2) MOE_LAUNCH(k_route_topk<2>, grid, 256, 0, st, logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride,
+                                 logits_out, topk_idx_out, topk_w_out);
+  else if (epl <= 4) MOE_LAUNCH(k_route_topk<4>, grid, 256, 0, st, logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride,
+                                 logits_out, topk_idx_out, topk_w_out);
+  else if (epl <= 8) MOE_LAUNCH(k_route_topk<8>, grid, 256, 0, st, logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride,
+                                 logits_out, topk_idx_out, topk_w_out);
+  else if (epl <= 16) MOE_LAUNCH(k_route_topk<16>, grid, 256, 0, st, logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride,
+                                 logits_out, topk_idx_out, topk_w_out);
+  else MOE_LAUNCH(k_route_topk<32>, grid, 256, 0, st, logits, bias, T, E, k, topk_idx, topk_w, masks, part, nsplit, part_stride,
+                                 logits_out, topk_idx_out, topk_w_out);
   return cudaGetLastError();
 }
 
 cudaError_t launch_route_scan(const uint64_t* masks, int C, int E, int* count, int* offset, int* pad_off,
                               int* tile_off, int* chunk_base, int* pair_of_row, int* user_offsets, cudaStream_t st,
                               int* order, int* tile_off2, int4* tile_rec, int4* ord_rec, int4* tile_rec2) {
-  k_route_scan<<<1, 1024, 0, st>>>(masks, C, E, count, offset, pad_off, tile_off, chunk_base, pair_of_row,
+  MOE_LAUNCH(k_route_scan, 1, 1024, 0, st, masks, C, E, count, offset, pad_off, tile_off, chunk_base, pair_of_row,
                                    user_offsets, order, tile_off2, tile_rec, ord_rec, tile_rec2);
   return cudaGetLastError();
 }
 
 cudaError_t launch_route_index(const uint64_t* masks, const int* chunk_base, const int* topk_idx, const int* offset,
                                const int* pad_off, int T, int E, int k, int* rowp_of_pair, int* row_of_pair,
-                               int* pair_of_row, cudaStream_t st) {
+                               int* pair_of_row, cudaStream_t st, int* row_of_pair_out) {
   const int C = (T + kChunk - 1) / kChunk;
   const size_t sm = E * (sizeof(uint64_t) + sizeof(int));
-  k_route_index<<<C, 256, sm, st>>>(masks, chunk_base, topk_idx, offset, pad_off, T, E, k, rowp_of_pair, row_of_pair,
-                                    pair_of_row);
+  MOE_LAUNCH(k_route_index, C, 256, sm, st, masks, chunk_base, topk_idx, offset, pad_off, T, E, k, rowp_of_pair,
+             row_of_pair, pair_of_row, row_of_pair_out);
   return cudaGetLastError();
 }
 
@@ -450,7 +481,7 @@ cudaError_t launch_gather_rows(const void* x, const int* pair_of_row, const int*
                                void* x_perm, float* xnorm, int num_sms, cudaStream_t st) {
   const int64_t want = (Rmax + 7) / 8;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 16));
-  k_gather_rows<TIO><<<grid, 256, 0, st>>>(reinterpret_cast<const TIO*>(x), pair_of_row, pad_total, H, k,
+  MOE_LAUNCH(k_gather_rows<TIO>, grid, 256, 0, st, reinterpret_cast<const TIO*>(x), pair_of_row, pad_total, H, k,
                                            reinterpret_cast<TIO*>(x_perm), xnorm);
   return cudaGetLastError();
 }
@@ -463,7 +494,7 @@ cudaError_t launch_combine(const void* y_pair, const int* rowp_of_pair, const fl
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_combine_k8, 256, 0) != cudaSuccess || per_sm < 1)
       per_sm = 1;
     const int g = (int)std::max<int64_t>(1, std::min<int64_t>(T, (int64_t)num_sms * per_sm));
-    k_combine_k8<<<g, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(y_pair), rowp_of_pair, topk_w,
+    MOE_LAUNCH(k_combine_k8, g, 256, 0, st, reinterpret_cast<const __nv_bfloat16*>(y_pair), rowp_of_pair, topk_w,
                                     reinterpret_cast<const __nv_bfloat16*>(sh_y), T, H, k,
                                     reinterpret_cast<__nv_bfloat16*>(y));
     return cudaGetLastError();
@@ -475,7 +506,7 @@ cudaError_t launch_combine(const void* y_pair, const int* rowp_of_pair, const fl
     const int64_t want = ((int64_t)T + 7) / 8;
     grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 16));
   }
-  k_combine<TIO><<<grid, 256, 0, st>>>(reinterpret_cast<const TIO*>(y_pair), rowp_of_pair, topk_w,
+  MOE_LAUNCH(k_combine<TIO>, grid, 256, 0, st, reinterpret_cast<const TIO*>(y_pair), rowp_of_pair, topk_w,
                                        reinterpret_cast<const TIO*>(sh_y), T, H, k, reinterpret_cast<TIO*>(y));
   return cudaGetLastError();
 }

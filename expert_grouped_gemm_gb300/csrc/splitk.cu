@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(256) k_splitk_store(const float* __restrict__ 
                                                       const int* __restrict__ nrows_dev, int nrows_const,
                                                       const int* __restrict__ pair_of_row, int N, int64_t ldo,
                                                       __nv_bfloat16* __restrict__ out) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const int nrows = nrows_dev ? *nrows_dev : nrows_const;
   const int nv = N / 8;
   for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < (int64_t)nrows * nv;
@@ -64,6 +65,7 @@ __global__ void __launch_bounds__(256) k_splitk_swiglu(const float* __restrict__
                                                        const int* __restrict__ nrows_dev,
                                                        const int* __restrict__ pair_of_row, int F,
                                                        __nv_bfloat16* __restrict__ ab, __nv_bfloat16* __restrict__ h) {
+  pdl_wait();  // the previous kernel has completed and its writes are visible
   const int nrows = *nrows_dev;
   const int nv = F / 8;
   for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < (int64_t)nrows * nv;
@@ -97,7 +99,7 @@ cudaError_t launch_splitk_store(const float* part, int64_t stride, int S, const 
                                 int64_t max_rows, const int* pair_of_row, int N, int64_t ldo, void* out, int num_sms,
                                 cudaStream_t st) {
   if (N % 8 || ldo % 8) return cudaErrorInvalidValue;
-  k_splitk_store<<<grid_rows(max_rows, N, num_sms), 256, 0, st>>>(part, stride, S, nrows_dev, nrows_const,
+  MOE_LAUNCH(k_splitk_store, grid_rows(max_rows, N, num_sms), 256, 0, st, part, stride, S, nrows_dev, nrows_const,
                                                                   pair_of_row, N, ldo,
                                                                   reinterpret_cast<__nv_bfloat16*>(out));
   return cudaGetLastError();
@@ -106,7 +108,7 @@ cudaError_t launch_splitk_store(const float* part, int64_t stride, int S, const 
 cudaError_t launch_splitk_swiglu(const float* part, int64_t stride, int S, const int* nrows_dev, int64_t max_rows,
                                  const int* pair_of_row, int F, void* ab, void* h, int num_sms, cudaStream_t st) {
   if (F % 8) return cudaErrorInvalidValue;
-  k_splitk_swiglu<<<grid_rows(max_rows, F, num_sms), 256, 0, st>>>(part, stride, S, nrows_dev, pair_of_row, F,
+  MOE_LAUNCH(k_splitk_swiglu, grid_rows(max_rows, F, num_sms), 256, 0, st, part, stride, S, nrows_dev, pair_of_row, F,
                                                                    reinterpret_cast<__nv_bfloat16*>(ab),
                                                                    reinterpret_cast<__nv_bfloat16*>(h));
   return cudaGetLastError();
