@@ -221,6 +221,37 @@ struct State {
 std::mutex g_mu;
 std::unordered_map<void*, State> g_state;
 
+// A stream of the workspace's own for the backward's router-gradient and dX-reduce
+// kernels, which run beside the dW GEMMs: forked from the caller's stream by `fork`
+// after the dX GEMMs and joined back by `join` before the router dW GEMM, so the
+// call's work stays ordered on (and capturable from) the caller's stream.
+#ifndef MOE_BWD_OVERLAP
+#define MOE_BWD_OVERLAP 1  // 0: every backward kernel on the caller's stream
+#endif
+struct Side {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::unordered_map<void*, Side> g_side;  // guarded by g_mu
+
+cudaError_t side_for(void* ws, Side* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Side& sd = g_side[ws];
+  if (!sd.s) {
+    cudaError_t e = cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      if (sd.fork) cudaEventDestroy(sd.fork);
+      if (sd.s) cudaStreamDestroy(sd.s);
+      sd = Side();
+      return e;
+    }
+  }
+  *out = sd;
+  return cudaSuccess;
+}
+
 bool same_dims(const moe_dims& a, const moe_dims& b) {
   return a.T == b.T && a.H == b.H && a.F == b.F && a.E == b.E && a.k == b.k && a.F_shared == b.F_shared &&
          a.dtype == b.dtype && a.flags == b.flags;
@@ -972,22 +1003,47 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
     b.out_rows = L.Tpad;
     CKL(run_gemm(b, bf, 256, st, sms));
   }
+  // The router gradient and the dX reduce touch nothing the dW GEMMs read or write, so
+  // they can run on the side stream beside the dW GEMMs. That pays while the dW GEMMs
+  // leave HBM bandwidth and power to spare, i.e. while the dW gate/up GEMM at the mean
+  // load of r = T k / E rows per expert sits below the ridge: r H 2F flops over
+  // 2 (r H + r 2F + H 2F) bytes against 1.94 PFLOP/s / 6.78 TB/s = 287 flop/B (GB300,
+  // bf16, measured). Kept on `st` while per-family timing is on, so that every span
+  // brackets its own kernels.
+  bool timing;
   {
-    Span sp(st, FAM_BW);
+    std::lock_guard<std::mutex> lk(g_timing.mu);
+    timing = g_timing.on;
+  }
+  const double r_mean = (double)L.P / (double)L.E;
+  const double dw_flop_per_byte = r_mean * (double)L.H * (2.0 * L.F) /
+                                  (r_mean * ((double)L.H + 2.0 * L.F) + (double)L.H * (2.0 * L.F));
+  const bool overlap = MOE_BWD_OVERLAP && !frozen && !timing && dw_flop_per_byte < 287.0;
+  Side side;
+  cudaStream_t bs = st;
+  if (overlap) {
+    CK(side_for(ws, &side));
+    CK(cudaEventRecord(side.fork, st));
+    CK(cudaStreamWaitEvent(side.s, side.fork, 0));
+    bs = side.s;
+  }
+  {
+    Span sp(bs, FAM_BW);
     if (bf) {
       CKL(launch_router_bwd<__nv_bfloat16>(p.g, p.rowp_of_pair, p.topk_idx, p.topk_w, T, (int)L.Tpad, E, k, p.dl_sel,
-                                          frozen ? nullptr : p.dl, sms, st));
-      CKL(launch_transpose<__nv_bfloat16>(s.w_router, H, E, p.wrT, st));
+                                          frozen ? nullptr : p.dl, sms, bs));
+      CKL(launch_transpose<__nv_bfloat16>(s.w_router, H, E, p.wrT, bs));
       CKL(launch_dx_reduce<__nv_bfloat16>(p.dx_pair, crow, p.topk_idx, p.dl_sel, p.wrT, shared ? p.sh_dx : nullptr, T,
-                                         H, k, dx, sms, st));
+                                         H, k, dx, sms, bs));
     } else {
       CKL(launch_router_bwd<float>(p.g, p.rowp_of_pair, p.topk_idx, p.topk_w, T, (int)L.Tpad, E, k, p.dl_sel,
-                                  frozen ? nullptr : p.dl, sms, st));
-      CKL(launch_transpose<float>(s.w_router, H, E, p.wrT, st));
+                                  frozen ? nullptr : p.dl, sms, bs));
+      CKL(launch_transpose<float>(s.w_router, H, E, p.wrT, bs));
       CKL(launch_dx_reduce<float>(p.dx_pair, crow, p.topk_idx, p.dl_sel, p.wrT, shared ? p.sh_dx : nullptr, T, H, k,
-                                 dx, sms, st));
+                                 dx, sms, bs));
     }
   }
+  if (overlap) CK(cudaEventRecord(side.join, bs));
   if (!frozen) {
     // dW_gate[e] = x_e^T da_e, dW_up[e] = x_e^T db_e   (rows of the group are the reduction)
     {
@@ -1039,7 +1095,8 @@ int moe_bwd(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream, const
       a.grp_rec = use_retained ? p.ret_ord_rec : p.ord_rec;
       CKL(run_gemm(a, bf, 256, st, sms));
     }
-    // dW_router = x^T dl
+    // dW_router = x^T dl (dl from the router gradient: the side stream joins here)
+    if (overlap) CK(cudaStreamWaitEvent(st, side.join, 0));
     {
       GemmArgs a = base_args(p.status);
       a.var_k = 1;

@@ -23,8 +23,12 @@
  *     (MOE_BF16 or MOE_F32); router_bias, top-k weights, logits and scores are
  *     float32; indices, offsets and quotas are int32. Accumulation is fp32.
  *   - stream is a cudaStream_t passed as void*. Every call only enqueues work
- *     on it and never synchronises the host (moe_read_status excepted), so a
- *     fwd / select / bwd sequence can be captured in a CUDA graph.
+ *     and never synchronises the host (moe_read_status excepted). moe_bwd runs
+ *     its router-gradient and dX-reduce kernels on a stream the library keeps
+ *     for the workspace, forked from `stream` and joined back into it with
+ *     events, so all of a call's work comes after earlier work on `stream` and
+ *     before later work on it, and a fwd / select / bwd sequence can be
+ *     captured in a CUDA graph.
  *   - Return values: MOE_OK or a negative moe_status. Arguments are validated
  *     on the host before anything is enqueued; on error nothing is enqueued
  *     and moe_last_error() describes the failure. Errors found by the GPU

@@ -79,3 +79,40 @@ def test_device_quota_planner_full_size():
     rep, g, _ = planned_parity_case(WORKLOADS["qwen3_t4096_full"], (1, 2), seed=0)
     assert rep["quota_sum"] == rep["R"]
     print(rep)
+
+
+# moe_bwd forks its router-gradient and dX-reduce kernels onto a stream of its own and
+# joins them back with events: a whole step captured in a CUDA graph and replayed must
+# give the eager step's results bit for bit.
+@pytest.mark.parametrize("quota", [False, True])
+def test_step_captured_in_a_cuda_graph_is_bitwise_equal(quota):
+    w = custom("graph_step", T=320, H=256, F=192, E=16, k=4, F_shared=128, zipf_s=1.0,
+               quota_factor=0.5 if quota else None)
+    inp = make_inputs(w, seed=3)
+    ref, _ = run_gpu(w, inp)
+    dev = torch.device("cuda")
+    layer = MoELayer(w, inp, dev, record_routing=True)
+    x = inp["x"].to(dev)
+    dy = inp["dy"].to(dev)
+    q = inp["quota"].to(dev) if quota else None
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.step(x, dy, q)  # first calls outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        layer.step(x, dy, q)
+    layer.y.zero_()
+    layer.dx.zero_()
+    for t in layer.grads.values():
+        t.zero_()
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert _lib.moe_read_status(layer.ws) == _lib.MOE_OK
+    f = lambda t: t.detach().float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(f(layer.y), ref["Y"])
+    assert np.array_equal(f(layer.dx), ref["dX"])
+    for n, t in layer.grads.items():
+        assert np.array_equal(f(t), ref[n]), n
