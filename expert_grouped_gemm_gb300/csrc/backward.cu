@@ -200,11 +200,10 @@ __global__ void __launch_bounds__(1024) k_ret_scan(const int* ret_count, int E, 
   const int pad = (cnt + 15) / 16 * 16;
   const int tiles = (cnt + 127) / 128;
   const int tiles2 = (cnt + 255) / 256;
-  int tc, tp, tt, tt2;
-  const int oc = block_excl_scan(cnt, &tc);
-  const int op = block_excl_scan(pad, &tp);
-  const int ot = block_excl_scan(tiles, &tt);
-  const int ot2 = block_excl_scan(tiles2, &tt2);
+  int4 tot;
+  const int4 ex = block_excl_scan4(make_int4(cnt, pad, tiles, tiles2), &tot);
+  const int oc = ex.x, op = ex.y, ot = ex.z, ot2 = ex.w;
+  const int tc = tot.x, tp = tot.y, tt = tot.z, tt2 = tot.w;
   if (ret_tile_off2 && e < E) ret_tile_off2[e] = ot2;
   if (ret_tile_off2 && e == 0) ret_tile_off2[E] = tt2;
   if (e < E) {

@@ -35,6 +35,12 @@ __global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* 
   float* lrow = logits + (int64_t)t * E;
   float v[EPL];
   float l[EPL];
+  float bv_[EPL];  // the bias, loaded beside the logits rather than after them
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    bv_[i] = (bias && e < E) ? bias[e] : 0.0f;
+  }
   if (part) {  // the router GEMM ran as a K split: its partial sums, added in split order
 #pragma unroll
     for (int i = 0; i < EPL; ++i) l[i] = 0.0f;
@@ -64,7 +70,7 @@ __global__ void __launch_bounds__(256) k_route_topk(float* logits, const float* 
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
-      const float x = l[i] + (bias ? bias[e] : 0.0f);
+      const float x = l[i] + bv_[i];
       lrow[e] = x;                     // the biased logits the selection used
       if (ulogits) ulogits[(int64_t)t * E + e] = x;
       v[i] = (x != x) ? -INFINITY : x;  // NaN ranks last
@@ -181,7 +187,13 @@ __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int 
   const int c0 = pp * per, c1 = min(C, c0 + per);
   int pc = 0;
   if (worker)
-    for (int c = c0; c < c1; ++c) pc += __popcll(masks[(int64_t)c * E + pe]);
+    for (int cb = c0; cb < c1; cb += 8) {  // eight mask loads in flight, then their popcounts
+      uint64_t m[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m[j] = cb + j < c1 ? masks[(int64_t)(cb + j) * E + pe] : 0ull;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) pc += __popcll(m[j]);
+    }
   if (worker) part_cnt[pp * E + pe] = pc;
   __syncthreads();
   const int e = tid;
@@ -192,11 +204,10 @@ __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int 
   const int pad = (cnt + 15) / 16 * 16;
   const int tiles = (cnt + 127) / 128;
   const int tiles2 = (cnt + 255) / 256;
-  int tot_c, tot_p, tot_t, tot_t2;
-  const int oc = block_excl_scan(e < E ? cnt : 0, &tot_c);
-  const int op = block_excl_scan(e < E ? pad : 0, &tot_p);
-  const int ot = block_excl_scan(e < E ? tiles : 0, &tot_t);
-  const int ot2 = block_excl_scan(e < E ? tiles2 : 0, &tot_t2);
+  int4 tot;
+  const int4 ex = block_excl_scan4(e < E ? make_int4(cnt, pad, tiles, tiles2) : make_int4(0, 0, 0, 0), &tot);
+  const int oc = ex.x, op = ex.y, ot = ex.z, ot2 = ex.w;
+  const int tot_c = tot.x, tot_p = tot.y, tot_t = tot.z, tot_t2 = tot.w;
   __shared__ int s_pad[1024];
   if (e < E) {
     count[e] = cnt;
@@ -224,9 +235,16 @@ __global__ void __launch_bounds__(1024) k_route_scan(const uint64_t* masks, int 
   if (worker) {
     int run = s_pad[pe];
     for (int p = 0; p < pp; ++p) run += part_cnt[p * E + pe];
-    for (int c = c0; c < c1; ++c) {
-      chunk_base[(int64_t)c * E + pe] = run;
-      run += __popcll(masks[(int64_t)c * E + pe]);
+    for (int cb = c0; cb < c1; cb += 8) {
+      uint64_t m[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m[j] = cb + j < c1 ? masks[(int64_t)(cb + j) * E + pe] : 0ull;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (cb + j < c1) {
+          chunk_base[(int64_t)(cb + j) * E + pe] = run;
+          run += __popcll(m[j]);
+        }
     }
   }
 }
