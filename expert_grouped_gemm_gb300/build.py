@@ -2,7 +2,7 @@
 
 Each .cu file under csrc/ is compiled in parallel to an object in _build/,
 then all objects are linked into expert_grouped_gemm_gb300/libmoe_gb300.so
-(CUDA runtime linked statically; the driver's tensor-map encoder is looked up
+(CUDA runtime linked statically; the CUDA driver's tensor-map encoder is looked up
 at run time, so no libcuda link is needed).
 """
 from __future__ import annotations
