@@ -1,5 +1,5 @@
 """The multi-process parts of bench.py on CPU: two gloo ranks (one process per GPU on a
-GPU machine; here plain processes) agree on the slowest rank's time, and the job's value is
+multi-GPU node; here plain processes) agree on the slowest rank's time, and the job's value is
 every rank's tokens over that time. The reference arm runs on rank 0 only."""
 import os
 import socket
