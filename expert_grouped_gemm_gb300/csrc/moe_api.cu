@@ -333,8 +333,16 @@ struct Span {
 enum { FAM_GEMM = 0, FAM_BW = 1 };
 
 // ------------------------------------------------------------------ GEMM helpers
+// 1: the variable-M store GEMMs (expert down, dX of the pairs) run weight-stationary on
+// CTA pairs (gemm_ws.cu) where their shapes allow. Parity-green, measured slower than the
+// single-CTA kernel at the Qwen3 shape, so off by default.
+#ifndef MOE_WS
+#define MOE_WS 0
+#endif
+
 cudaError_t run_gemm(const GemmArgs& a, int bf16, int bn, cudaStream_t st, int sms) {
   Span sp(st, FAM_GEMM);
+  if (bf16 && MOE_WS && bn == 256 && ws_store_supported(a)) return launch_ws_store(a, st, sms);
   if (bf16) return launch_tc_gemm(a, bn, st, sms, 0);
   return launch_simt_gemm_f32(a, st);
 }
