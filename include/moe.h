@@ -28,7 +28,9 @@
  *     for the workspace, forked from `stream` and joined back into it with
  *     events, so all of a call's work comes after earlier work on `stream` and
  *     before later work on it, and a fwd / select / bwd sequence can be
- *     captured in a CUDA graph.
+ *     captured in a CUDA graph (make a workspace's first moe_bwd call outside
+ *     a capture: it creates that stream). The stream and its two events live as
+ *     long as the process.
  *   - Return values: MOE_OK or a negative moe_status. Arguments are validated
  *     on the host before anything is enqueued; on error nothing is enqueued
  *     and moe_last_error() describes the failure. Errors found by the GPU
